@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-output-channel scaled FP8 linear layer on GB300.
+
+One step = one call of the layer (one kernel launch) over one batch of
+synthetic input already resident in HBM.  The headline workload is the
+square prefill GEMM M = N = K = 4096 (seed 1); its throughput in TFLOP/s is
+`value`.  Successive steps rotate through enough copies of the operands that
+the working set is more than twice the L2 cache, so no step reads another
+step's operands from L2.
+
+Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload
+(independent problems, weak scaling, no collective on the data path); the
+time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 GEMM TFLOP/s (GB/s at M=32) per config; fraction of GB300 roofline"
+HEADLINE = "square"
+FP8_OVER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TC_SOURCES = ["fp8_channel_scaled_gb300/csrc/gemm_tc.cu", "fp8_channel_scaled_gb300/csrc/ptx.cuh",
+              "fp8_channel_scaled_gb300/csrc/realign.cuh"]
+DEC_SOURCES = ["fp8_channel_scaled_gb300/csrc/gemm_decode.cu",
+               "fp8_channel_scaled_gb300/csrc/ptx.cuh", "fp8_channel_scaled_gb300/csrc/realign.cuh"]
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` across ranks (a host scalar; not on the data path)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha(paths) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, paths):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    fn = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        text = open(fn).read()
+    except OSError:
+        return None
+    sha = sources_sha(paths)
+    for m in re.finditer(r"^\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*(\d+)\s*\|", text, re.M):
+        if m.group(1) == workload and m.group(2) == sha:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms while the timed region runs."""
+
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1].lower():
+                continue
+            rows.append((t, parts))
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        used = inside or rows
+        mhz = [float(r[1][2]) for r in used if r[1][2].replace(".", "").isdigit()]
+        max_mhz = [float(r[1][3]) for r in used if r[1][3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in used for n, v in zip(names, r[1][6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(max_mhz) if max_mhz else None,
+                "reasons": reasons, "samples": len(used), "in_timed_region": bool(inside)}
+
+
+# ---------------------------------------------------------------- workload on the device
+def rotation_count(bytes_per_set: int, l2_bytes: int, cap: int = 64) -> int:
+    """Copies of the operands so that the rotation covers more than 2x L2."""
+    return max(2, min(cap, math.ceil(2 * l2_bytes / max(bytes_per_set, 1)) + 1))
+
+
+def prepare(key: str, device, l2_bytes: int, rotate: bool = True):
+    import torch
+    import synth
+    wl = synth.WORKLOADS[key]
+    x, w, s = synth.workload_inputs(key)
+    xd = torch.from_numpy(x).to(device)
+    wd = torch.from_numpy(w).to(device)
+    sd = torch.from_numpy(s).to(device)
+    per_set = x.nbytes + w.nbytes + s.nbytes + 2 * wl.M * wl.N
+    n = rotation_count(per_set, l2_bytes) if rotate else 1
+    sets = []
+    for i in range(n):
+        sets.append((xd if i == 0 else xd.clone(), wd if i == 0 else wd.clone(),
+                     sd if i == 0 else sd.clone(),
+                     torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=device)))
+    return wl, (x, w, s), sets, per_set
+
+
+def time_steps(sets, steps: int, warmup: int, stream, call):
+    """Warm up, then time `steps` launches back to back with CUDA events on
+    `stream`; returns (region seconds, per-launch seconds list)."""
+    import torch
+    for i in range(warmup):
+        call(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        call(*sets[i % len(sets)])
+        ev[i][1].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    return region0.elapsed_time(region1) / 1e3, per
+
+
+def cpu_baseline(x, w, s, wl, target_s: float = 12.0, rows=None):
+    """Time the oracle on a bounded sample of the workload's rows."""
+    import numpy as np
+    import oracle
+    cores = oracle.default_threads()
+    probe_rows = np.arange(min(wl.M, max(1, cores // 2)), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.linear_rows(x, w, s, probe_rows)
+    t_probe = time.perf_counter() - t0
+    per_row = t_probe / probe_rows.size
+    if rows is None:
+        n = int(max(1, min(wl.M, target_s / max(per_row, 1e-9))))
+        n = max(cores, (n // cores) * cores) if n >= cores else n
+        n = min(n, wl.M)
+        rows = np.linspace(0, wl.M - 1, n).round().astype(np.int64)
+    t0 = time.perf_counter()
+    y = oracle.linear_rows(x, w, s, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows.size * wl.N * wl.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows.size} of {wl.M} rows (full N={wl.N}, K={wl.K}), {dt:.1f} s",
+            "seconds": dt}, rows, y
+
+
+def bench_workload(key, steps, warmup, device, l2_bytes, stream, fg):
+    wl, host, sets, per_set = prepare(key, device, l2_bytes, rotate=(key != "small"))
+    call = lambda x, w, s, y: fg.fp8_gemm_scaled(x, w, s, y, stream)  # noqa: E731
+    region, per = time_steps(sets, steps, warmup, stream, call)
+    fg.check_device_error(stream)
+    return wl, host, sets, region, per, per_set
+
+
+# ---------------------------------------------------------------- arms
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local if torch.cuda.device_count() > local else 0)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    from fp8_channel_scaled_gb300 import build
+    build.build()
+    import fp8_channel_scaled_gb300 as fg
+
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+
+    # ---- headline workload, timed region with clock sampling
+    sampler = ClockSampler(str(getattr(props, "uuid", "")) if rank == 0 else None)
+    if rank == 0:
+        sampler.start()
+    wl, host, sets, per_set = prepare(HEADLINE, device, l2)
+    call = lambda x, w, s, y: fg.fp8_gemm_scaled(x, w, s, y, stream)  # noqa: E731
+    for i in range(args.warmup):
+        call(*sets[i % len(sets)])
+    torch.cuda.synchronize(device)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    r0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        call(*sets[i % len(sets)])
+        ev[i][1].record(stream)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark("t1")
+    barrier(device)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if rank == 0 else None
+    fg.check_device_error(stream)
+    region = r0.elapsed_time(r1) / 1e3
+    per = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    region_max = max_over_ranks(region, device)
+    flops = float(wl.flops)
+    value = world * args.steps * flops / region_max / 1e12
+    kern = statistics.mean(per)
+    plan = fg.plan(wl.M, wl.N, wl.K, x=sets[0][0], w=sets[0][1])
+
+    # ---- end to end through the public API from pinned host buffers
+    x_h, w_h, s_h = host
+    xp = torch.from_numpy(x_h).pin_memory()
+    wp = torch.from_numpy(w_h).pin_memory()
+    sp = torch.from_numpy(s_h).pin_memory()
+    yp = torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory()
+    xd, wd, sd, yd = sets[0]
+    e2e_steps = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        xd.copy_(xp, non_blocking=True)
+        wd.copy_(wp, non_blocking=True)
+        sd.copy_(sp, non_blocking=True)
+        fg.fp8_gemm_scaled(xd, wd, sd, yd, stream)
+        yp.copy_(yd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    fg.check_device_error(stream)
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
+    e2e = {"value": world * e2e_steps * flops / e2e_t / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(x_h.nbytes + w_h.nbytes + s_h.nbytes),
+           "d2h_bytes_per_step": int(2 * wl.M * wl.N), "steps": e2e_steps}
+
+    # ---- roofline of the dominant (only) kernel
+    peak_tf = peaks["bf16_tflops"] * FP8_OVER_BF16
+    achieved = flops / kern / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_tf, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                "traffic": recorded_traffic(HEADLINE, TC_SOURCES),
+                "algorithmic_bytes": int(wl.algorithmic_bytes),
+                "kernel_us": round(kern * 1e6, 3),
+                "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} (fp8/bf16 nominal)",
+                "frac_nominal_4500": round(achieved / 4500.0, 4)}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(region_max / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
+            "data": "synthetic (seeded numpy PCG64 draws quantised to E4M3)",
+            "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "seed": wl.seed,
+                       "path": "main" if plan.path == fg.PATH_MAIN else "decode",
+                       "tile": f"{plan.tile_m}x{plan.tile_n}x128", "stages": plan.stages,
+                       "grid": plan.grid, "parallelism": f"replicas x{world}",
+                       "l2": f"rotating {len(sets)} operand sets ({len(sets) * per_set / 2**20:.0f} MiB > 2x L2 {l2 / 2**20:.0f} MiB), no flush kernel"},
+            "roofline": roofline, "gpu_launches": args.steps * plan.launches, "e2e": e2e,
+            "clocks": clocks}
+
+    # ---- the other workloads (parity cases; reported for context)
+    if rank == 0 and not args.headline_only:
+        others = {}
+        for key in ("small", "decode", "oddk", "mlp"):
+            st = {"small": 2000, "decode": 400, "oddk": 400, "mlp": 60}[key]
+            wl2, _, sets2, region2, per2, per_set2 = bench_workload(key, st, 10, device, l2, stream, fg)
+            k2 = statistics.median(per2)
+            tf = wl2.flops / k2 / 1e12
+            gbs = wl2.algorithmic_bytes / k2 / 1e9
+            roof_t = max(wl2.flops / 4.5e15, wl2.algorithmic_bytes / 8e12)
+            p2 = fg.plan(wl2.M, wl2.N, wl2.K, x=sets2[0][0], w=sets2[0][1])
+            others[key] = {"workload": wl2.name, "us_median": round(k2 * 1e6, 2),
+                           "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1),
+                           "frac_roofline_nominal": round(roof_t / k2, 4),
+                           "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
+                           "frac_fp8_measured": round(tf / peak_tf, 4),
+                           "path": "main" if p2.path == fg.PATH_MAIN else "decode",
+                           "splits": p2.splits, "realign": p2.realign,
+                           "l2": "no rotation (launch-bound)" if key == "small" else f"rotating {len(sets2)} sets"}
+            del sets2
+            torch.cuda.empty_cache()
+        line["workloads"] = others
+
+    # ---- CPU baseline (oracle on host cores, bounded sample) and a parity check of that sample
+    if rank == 0 and not args.no_cpu_baseline:
+        x_h, w_h, s_h = host
+        cb, rows, yref = cpu_baseline(x_h, w_h, s_h, wl, target_s=args.cpu_seconds)
+        cb.pop("seconds")
+        line["cpu_baseline"] = cb
+        import numpy as np
+        got = sets[0][3][torch.from_numpy(rows).to(device)].view(torch.int16).cpu().numpy().view(np.uint16)
+        g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        r = (yref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        bad = int(np.sum(np.abs(g - r) > 2.0 ** -7 * np.abs(r) + 1e-3))
+        line["parity_sample"] = {"rows": int(rows.size), "elements": int(r.size), "outside_tolerance": bad}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores; one bounded sample
+    of the headline workload per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    wl = synth.WORKLOADS[HEADLINE]
+    x, w, s = synth.workload_inputs(HEADLINE)
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.linear_rows(x, w, s, np.arange(cores, dtype=np.int64))
+    per_row = (time.perf_counter() - t0) / cores
+    total = args.steps + args.warmup
+    rows_per_step = int(max(1, min(wl.M, args.cpu_seconds * 4 / max(total, 1) / max(per_row, 1e-9))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.linear_rows(x, w, s, rng.integers(0, wl.M, rows_per_step))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.linear_rows(x, w, s, rng.integers(0, wl.M, rows_per_step))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * wl.N * wl.K * args.steps
+    value = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (exact dot, one bf16 rounding)",
+            "data": "synthetic (seeded numpy PCG64 draws quantised to E4M3)",
+            "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "seed": wl.seed,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step} random rows of {wl.M} per step (full N, K)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the context timings of the other four workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU seconds spent in the oracle sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+"""ctypes marshalling for include/fp8_gemm.h.  No computation happens here."""
+from __future__ import annotations
+
+import ctypes
+import threading
+from dataclasses import dataclass
+from pathlib import Path
+
+_PKG = Path(__file__).resolve().parent
+_LIB_PATH = _PKG / "_lib" / "libfp8gemm.so"
+
+PATH_AUTO, PATH_MAIN, PATH_DECODE = 0, 1, 2
+STATUS = {0: "OK", 1: "EINVAL", 2: "EALIGN", 3: "EDEVICE", 4: "ELAUNCH", 5: "ETIMEOUT",
+          6: "EUNSUPPORTED"}
+
+
+class FP8GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = f"{what}: " if what else ""
+        super().__init__(f"{msg}{STATUS.get(status, status)} ({_status_string(status)})")
+
+
+class _COptions(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("force_realign", ctypes.c_int),
+                ("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("splits", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
+
+
+class _CPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
+        "threads", "smem_bytes", "launches")]
+
+
+@dataclass
+class Options:
+    path: int = PATH_AUTO
+    force_realign: bool = False
+    tile_n: int = 0
+    stages: int = 0
+    splits: int = 0
+
+    def _c(self) -> _COptions:
+        o = _COptions()
+        o.path, o.force_realign = int(self.path), int(bool(self.force_realign))
+        o.tile_n, o.stages, o.splits = int(self.tile_n), int(self.stages), int(self.splits)
+        return o
+
+
+@dataclass
+class Plan:
+    path: int
+    realign: int
+    tile_m: int
+    tile_n: int
+    stages: int
+    splits: int
+    grid: int
+    cluster: int
+    threads: int
+    smem_bytes: int
+    launches: int
+
+
+_lock = threading.RLock()
+_lib = None
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _LIB_PATH.exists():
+            raise FP8GemmError(3, f"CUDA library not built ({_LIB_PATH}); run "
+                               "fp8_channel_scaled_gb300.build.build()")
+        L = ctypes.CDLL(str(_LIB_PATH))
+        vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+        L.fp8_gemm_scaled.argtypes = [vp, vp, vp, vp, i, i, i, st]
+        L.fp8_gemm_scaled_ex.argtypes = [vp, vp, vp, vp, i, i, i, ctypes.POINTER(_COptions), st]
+        L.fp8_gemm_plan.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions),
+                                    ctypes.POINTER(_CPlan)]
+        L.fp8_gemm_check_device_error.argtypes = [st]
+        L.fp8_gemm_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
+        L.fp8_gemm_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, st]
+        L.fp8_gemm_status_string.argtypes = [i]
+        L.fp8_gemm_status_string.restype = ctypes.c_char_p
+        L.fp8_gemm_last_device_error_bits.argtypes = []
+        L.fp8_gemm_last_device_error_bits.restype = ctypes.c_uint
+        for f in ("fp8_gemm_scaled", "fp8_gemm_scaled_ex", "fp8_gemm_plan",
+                  "fp8_gemm_check_device_error", "fp8_gemm_set_wait_budget_ns",
+                  "fp8_gemm_selftest_wait_timeout", "fp8_gemm_version"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _status_string(status: int) -> str:
+    if _lib is None:
+        return "library not loaded"
+    return _lib.fp8_gemm_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int:
+    return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+
+
+def _shapes(x, w, scale, y):
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"x {tuple(x.shape)} and w {tuple(w.shape)} must be [M,K] and [N,K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if tuple(scale.shape) != (N,) or tuple(y.shape) != (M, N):
+        raise ValueError(f"scale {tuple(scale.shape)} / y {tuple(y.shape)} do not match M={M} N={N}")
+    for name, t in (("x", x), ("w", w), ("scale", scale), ("y", y)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if x.element_size() != 1 or w.element_size() != 1:
+        raise TypeError("x and w must be 1-byte E4M3 tensors (uint8 or float8_e4m3fn)")
+    if scale.element_size() != 4 or y.element_size() != 2:
+        raise TypeError("scale must be float32 and y bfloat16")
+    return int(M), int(N), int(K)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise FP8GemmError(status, what)
+
+
+# ---------------------------------------------------------------- same names as the C ABI
+def fp8_gemm_scaled(x, w, scale, y, stream=None) -> None:
+    """y = bf16((x . w^T, fp32 acc) * scale) on `stream` (torch tensors on one GPU)."""
+    M, N, K = _shapes(x, w, scale, y)
+    _check(lib().fp8_gemm_scaled(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
+                                 _stream_handle(stream)), "fp8_gemm_scaled")
+
+
+def fp8_gemm_scaled_ex(x, w, scale, y, options: Options | None = None, stream=None) -> None:
+    M, N, K = _shapes(x, w, scale, y)
+    o = (options or Options())._c()
+    _check(lib().fp8_gemm_scaled_ex(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
+                                    ctypes.byref(o), _stream_handle(stream)), "fp8_gemm_scaled_ex")
+
+
+def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None = None,
+                  x_ptr: int = 0, w_ptr: int = 0) -> Plan:
+    o = (options or Options())._c()
+    p = _CPlan()
+    _check(lib().fp8_gemm_plan(int(device), x_ptr or None, w_ptr or None, int(M), int(N), int(K),
+                               ctypes.byref(o), ctypes.byref(p)), "fp8_gemm_plan")
+    return Plan(*[getattr(p, f[0]) for f in _CPlan._fields_])
+
+
+def fp8_gemm_check_device_error(stream=None) -> int:
+    """Synchronise `stream`, read and clear the device error word; returns the status."""
+    return int(lib().fp8_gemm_check_device_error(_stream_handle(stream)))
+
+
+def fp8_gemm_set_wait_budget_ns(ns: int) -> None:
+    _check(lib().fp8_gemm_set_wait_budget_ns(int(ns)), "fp8_gemm_set_wait_budget_ns")
+
+
+def fp8_gemm_selftest_wait_timeout(budget_ns: int, stream=None) -> None:
+    _check(lib().fp8_gemm_selftest_wait_timeout(int(budget_ns), _stream_handle(stream)),
+           "fp8_gemm_selftest_wait_timeout")
+
+
+def fp8_gemm_status_string(status: int) -> str:
+    return _status_string(status)
+
+
+def fp8_gemm_version() -> int:
+    return int(lib().fp8_gemm_version())
+
+
+# ---------------------------------------------------------------- conveniences
+def check_device_error(stream=None) -> None:
+    """Raise if a kernel launched since the last check gave up a bounded wait."""
+    st = fp8_gemm_check_device_error(stream)
+    if st != 0:
+        bits = int(lib().fp8_gemm_last_device_error_bits())
+        raise FP8GemmError(st, f"device error bits 0x{bits:x}")
+
+
+def plan(M: int, N: int, K: int, options: Options | None = None, device: int | None = None,
+         x=None, w=None) -> Plan:
+    if device is None:
+        import torch
+        device = torch.cuda.current_device()
+    return fp8_gemm_plan(device, M, N, K, options, _ptr(x) if x is not None else 0,
+                         _ptr(w) if w is not None else 0)
+
+
+def linear(x, w, scale, out=None, options: Options | None = None, stream=None):
+    """Allocate (or reuse `out`) and return y = bf16((x . w^T) * scale)."""
+    import torch
+    if out is None:
+        out = torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device=x.device)
+    if options is None:
+        fp8_gemm_scaled(x, w, scale, out, stream)
+    else:
+        fp8_gemm_scaled_ex(x, w, scale, out, options, stream)
+    return out

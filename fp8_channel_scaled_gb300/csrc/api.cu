@@ -1,0 +1,449 @@
+// api.cu -- the C ABI of include/fp8_gemm.h: argument validation, path
+// selection, TMA descriptor encoding, launch, and the device error word.
+//
+// Path selection follows the regimes the pages' submissions pin instead of
+// autotuning ("glm-5.2" page: dense tiles plus a skinny config for M <= 64;
+// "claude-fable-5" page, Triton paragraph: split-K for M <= 64): M <= 64
+// takes the split-K decode kernel, everything else the persistent tile
+// kernel.  Rows that TMA cannot describe (pitch not a multiple of 16 bytes,
+// or a base not 16-byte aligned) switch either kernel to its realigning
+// producer.  Nothing derived from operand data is cached.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fp8_gemm.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8g {
+namespace {
+
+// Device error word: kernels OR error bits into it; the host reads and clears
+// it in fp8_gemm_check_device_error.
+__device__ unsigned g_device_error_word;
+
+// One thread waits for an mbarrier phase that nothing completes.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1u);
+  abort_flag = 0;
+  fence_mbar_init();
+  const WaitCtx wc{err, &abort_flag, budget_ns};
+  (void)mbar_wait_bounded(b, 0u, wc, kErrWaitSelfTest);
+}
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultBudgetNs = 1000000000ull;
+
+struct DevState {
+  bool init = false;
+  int status = FP8GEMM_OK;
+  int sm_count = 0;
+  int smem_optin = 0;
+  unsigned* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+unsigned long long g_budget_ns = 0;
+unsigned g_last_error_bits = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+unsigned long long budget_ns() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_budget_ns == 0) {
+    g_budget_ns = kDefaultBudgetNs;
+    if (const char* s = std::getenv("FP8GEMM_WAIT_BUDGET_NS")) {
+      const unsigned long long v = std::strtoull(s, nullptr, 10);
+      if (v > 0) g_budget_ns = v;
+    }
+  }
+  return g_budget_ns;
+}
+
+// Per-device set-up, once: properties, error word address, kernel attributes.
+int device_state(int dev, DevState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return FP8GEMM_EDEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (d.init) {
+    *out = &d;
+    return d.status;
+  }
+  d.init = true;
+  d.status = FP8GEMM_EDEVICE;
+  int major = 0, minor = 0;
+  if (cudaSetDevice(dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    *out = &d;
+    return d.status;
+  }
+  if (major != 10 || minor != 3) {  // the library is built for sm_103a only
+    *out = &d;
+    return d.status;
+  }
+  d.status = FP8GEMM_ELAUNCH;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err_word), g_device_error_word) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    *out = &d;
+    return d.status;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      *out = &d;
+      return d.status;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const int bns[] = {128, 256};
+  const int tc_stages[] = {3, 4, 6};
+  for (bool r : {false, true}) {
+    for (int bn : bns)
+      for (int s : tc_stages)
+        if (tc_config_supported(bn, s, r) && tc_prepare(bn, s, r) != cudaSuccess) {
+          cudaGetLastError();
+          *out = &d;
+          return d.status;
+        }
+    for (int mp : {32, 64, 128})
+      for (int s : {2, 3, 4, 6})
+        if (dec_config_supported(mp, s, r) && dec_prepare(mp, s, r) != cudaSuccess) {
+          cudaGetLastError();
+          *out = &d;
+          return d.status;
+        }
+  }
+  d.status = FP8GEMM_OK;
+  *out = &d;
+  return d.status;
+}
+
+// TMA descriptor of a row-major byte matrix [rows, K], box [box_rows, 128],
+// 128-byte swizzle, out-of-bounds elements read as zero.
+int encode_operand(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8GEMM_OK : FP8GEMM_ELAUNCH;
+}
+
+struct Plan {
+  fp8gemm_plan pub;
+  TcConfig tc;
+  DecConfig dec;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resident decode CTAs per SM, or 0 if the configuration cannot run.  The
+// tensor-memory budget (512 columns per SM) must cover every resident CTA, or
+// a CTA's allocation would wait for another CTA to finish.
+int dec_occupancy(const DevState& d, int mp, int stages, bool realign) {
+  const int smem = dec_smem_bytes(mp, stages, realign);
+  if (smem < 0 || smem > d.smem_optin) return 0;
+  int blocks = 0;
+  if (dec_blocks_per_sm(mp, stages, realign, &blocks) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (blocks * dec_tmem_cols(mp) > 512) return 0;
+  return blocks;
+}
+
+int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int K,
+              const fp8gemm_options* opt, Plan* pl) {
+  fp8gemm_options o{};
+  if (opt) o = *opt;
+  for (int r : o.reserved)
+    if (r != 0) return FP8GEMM_EINVAL;
+  std::memset(pl, 0, sizeof(*pl));
+  if (M == 0 || N == 0) return FP8GEMM_OK;  // nothing to do
+  const bool tma_ok = (K % 16 == 0) && (!x || aligned16(x)) && (!w || aligned16(w));
+  // K == 0 has nothing to load; the realigning variant then issues no copy
+  // and needs no tensor map.
+  const bool realign = o.force_realign != 0 || !tma_ok || K == 0;
+  const int num_kb = (K + 127) / 128;
+  int path = o.path;
+  if (path == FP8GEMM_PATH_AUTO) path = (M <= 64) ? FP8GEMM_PATH_DECODE : FP8GEMM_PATH_MAIN;
+  if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
+  pl->pub.path = path;
+  pl->pub.realign = realign ? 1 : 0;
+  pl->pub.launches = 1;
+
+  if (path == FP8GEMM_PATH_MAIN) {
+    int bn = o.tile_n;
+    if (bn == 0) bn = (N <= 128) ? 128 : 256;
+    if (bn != 128 && bn != 256) return FP8GEMM_EUNSUPPORTED;
+    int stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
+    if (!tc_config_supported(bn, stages, realign) ||
+        tc_smem_bytes(bn, stages, realign) > d.smem_optin)
+      return FP8GEMM_EUNSUPPORTED;
+    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + bn - 1) / bn);
+    pl->tc.bn = bn;
+    pl->tc.stages = stages;
+    pl->tc.realign = realign;
+    pl->tc.grid = static_cast<int>(std::min<long long>(tiles, d.sm_count));
+    pl->tc.group_m = 16;
+    pl->pub.tile_m = 128;
+    pl->pub.tile_n = bn;
+    pl->pub.stages = stages;
+    pl->pub.splits = 1;
+    pl->pub.grid = pl->tc.grid;
+    pl->pub.cluster = 1;
+    pl->pub.threads = tc_threads(realign);
+    pl->pub.smem_bytes = tc_smem_bytes(bn, stages, realign);
+    return FP8GEMM_OK;
+  }
+
+  // decode path
+  if (M > 128) return FP8GEMM_EUNSUPPORTED;
+  const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
+  const int n_tiles = (N + 127) / 128;
+  int best_s = 0, best_stages = 0;
+  double best_cost = 1e300;
+  const int stage_opts[] = {2, 3, 4, 6};
+  for (int stages : stage_opts) {
+    if (o.stages && stages != o.stages) continue;
+    if (!dec_config_supported(mp, stages, realign)) continue;
+    const int occ = dec_occupancy(d, mp, stages, realign);
+    if (occ <= 0) continue;
+    const long long slots = static_cast<long long>(occ) * d.sm_count;
+    const int s_max = std::max(1, std::min(8, num_kb));
+    for (int s = 1; s <= s_max; ++s) {
+      if (o.splits && s != o.splits) continue;
+      const long long ctas = static_cast<long long>(n_tiles) * s;
+      const long long waves = (ctas + slots - 1) / slots;
+      const int per_cta = (num_kb + s - 1) / s;
+      // a wave costs its longest CTA; shallow pipelines cost a little more
+      const double cost = static_cast<double>(waves) * (std::max(per_cta, 1) + 0.5 + 2.0 / stages);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_s = s;
+        best_stages = stages;
+      }
+    }
+  }
+  if (best_s == 0) return FP8GEMM_EUNSUPPORTED;
+  pl->dec.mp = mp;
+  pl->dec.stages = best_stages;
+  pl->dec.realign = realign;
+  pl->dec.splits = best_s;
+  pl->dec.n_tiles = n_tiles;
+  pl->pub.tile_m = 128;
+  pl->pub.tile_n = mp;
+  pl->pub.stages = best_stages;
+  pl->pub.splits = best_s;
+  pl->pub.grid = n_tiles * best_s;
+  pl->pub.cluster = best_s;
+  pl->pub.threads = dec_threads(realign);
+  pl->pub.smem_bytes = dec_smem_bytes(mp, best_stages, realign);
+  return FP8GEMM_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return na && nb && pa < pb + nb && pb < pa + na;
+}
+
+// Device of a device-accessible allocation, or -1 for host / unknown memory.
+int pointer_device(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return -1;
+  return a.device;
+}
+
+}  // namespace
+}  // namespace fp8g
+
+using namespace fp8g;
+
+extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* scale, void* y,
+                                  int M, int N, int K, const fp8gemm_options* opt,
+                                  fp8gemm_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8GEMM_EINVAL;
+  if (M == 0 || N == 0) return FP8GEMM_OK;
+  if (!scale || !y || (K > 0 && (!x || !w))) return FP8GEMM_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+    return FP8GEMM_EALIGN;
+  const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K);
+  const size_t wb = static_cast<size_t>(N) * static_cast<size_t>(K);
+  const size_t yb = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
+  const size_t sb = static_cast<size_t>(N) * 4u;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb))
+    return FP8GEMM_EINVAL;
+  const int dev = pointer_device(y);
+  if (dev < 0 || pointer_device(scale) != dev || (K > 0 && (pointer_device(x) != dev ||
+                                                           pointer_device(w) != dev)))
+    return FP8GEMM_EINVAL;
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  Plan pl;
+  st = make_plan(*d, x, w, M, N, K, opt, &pl);
+  if (st != FP8GEMM_OK) return st;
+
+  GemmArgs a{};
+  a.x = static_cast<const uint8_t*>(x);
+  a.w = static_cast<const uint8_t*>(w);
+  a.scale = scale;
+  a.y = static_cast<uint16_t*>(y);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_kb = (K + 127) / 128;
+  a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
+  a.err = d->err_word;
+  a.budget_ns = budget_ns();
+
+  // TMA descriptors are only meaningful on the TMA path (and need K >= 1);
+  // the realigning producer reads x and w through plain pointers.
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  const bool use_tma = !pl.pub.realign && K > 0;
+  cudaError_t e;
+  if (pl.pub.path == FP8GEMM_PATH_MAIN) {
+    if (use_tma) {
+      if (encode_operand(&tmA, x, M, K, 128) != FP8GEMM_OK ||
+          encode_operand(&tmB, w, N, K, pl.tc.bn) != FP8GEMM_OK)
+        return FP8GEMM_ELAUNCH;
+    }
+    e = launch_tc(tmA, tmB, a, pl.tc, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    if (use_tma) {
+      if (encode_operand(&tmA, w, N, K, 128) != FP8GEMM_OK ||
+          encode_operand(&tmB, x, M, K, pl.dec.mp) != FP8GEMM_OK)
+        return FP8GEMM_ELAUNCH;
+    }
+    e = launch_decode(tmA, tmB, a, pl.dec, reinterpret_cast<cudaStream_t>(stream));
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  return FP8GEMM_OK;
+}
+
+extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,
+                               int N, int K, fp8gemm_stream_t stream) {
+  return fp8_gemm_scaled_ex(x, w, scale, y, M, N, K, nullptr, stream);
+}
+
+extern "C" int fp8_gemm_plan(int device, const void* x, const void* w, int M, int N, int K,
+                             const fp8gemm_options* opt, fp8gemm_plan* out) {
+  if (!out || M < 0 || N < 0 || K < 0) return FP8GEMM_EINVAL;
+  DevState* d = nullptr;
+  int st = device_state(device, &d);
+  if (st != FP8GEMM_OK) return st;
+  Plan pl;
+  st = make_plan(*d, x, w, M, N, K, opt, &pl);
+  if (st != FP8GEMM_OK) return st;
+  *out = pl.pub;
+  return FP8GEMM_OK;
+}
+
+extern "C" int fp8_gemm_check_device_error(fp8gemm_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_EDEVICE;
+  }
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  unsigned bits = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpy(&bits, d->err_word, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(d->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_last_error_bits = bits;
+  }
+  return bits ? FP8GEMM_ETIMEOUT : FP8GEMM_OK;
+}
+
+extern "C" unsigned fp8_gemm_last_device_error_bits(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_last_error_bits;
+}
+
+extern "C" int fp8_gemm_set_wait_budget_ns(unsigned long long ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_budget_ns = ns ? ns : kDefaultBudgetNs;
+  return FP8GEMM_OK;
+}
+
+extern "C" int fp8_gemm_selftest_wait_timeout(unsigned long long budget, fp8gemm_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_EDEVICE;
+  }
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (budget == 0 || budget > 10000000000ull) return FP8GEMM_EINVAL;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(d->err_word, budget);
+  if (cudaGetLastError() != cudaSuccess) return FP8GEMM_ELAUNCH;
+  return FP8GEMM_OK;
+}
+
+extern "C" const char* fp8_gemm_status_string(int status) {
+  switch (status) {
+    case FP8GEMM_OK: return "ok";
+    case FP8GEMM_EINVAL: return "invalid argument (null or host pointer, bad size, y aliases an input)";
+    case FP8GEMM_EALIGN: return "misaligned pointer (scale needs 4 bytes, y needs 2 bytes)";
+    case FP8GEMM_EDEVICE: return "no usable device (needs compute capability 10.3)";
+    case FP8GEMM_ELAUNCH: return "CUDA launch or runtime call failed";
+    case FP8GEMM_ETIMEOUT: return "a kernel gave up a bounded wait; its output is invalid";
+    case FP8GEMM_EUNSUPPORTED: return "requested configuration is not built";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fp8_gemm_version(void) { return FP8GEMM_VERSION; }

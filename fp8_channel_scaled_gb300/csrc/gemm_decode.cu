@@ -1,0 +1,382 @@
+// gemm_decode.cu -- split-K tcgen05 kernel for skinny M (decode), for the
+// scaled FP8 linear layer  y = bf16((x_e4m3 . w_e4m3^T, fp32 acc) * scale[n]).
+//
+// With M <= 64 the layer is a weight stream: every byte of w is used once
+// and the arithmetic is small.  The pages' submissions use split-K with fp32
+// partials for skinny M and reduce them in a second step ("Kimi K3 (256k)"
+// page, SM90 and SM120 paragraphs: atomicAdd partials and a separate scaled
+// finalize kernel; "claude-fable-5" page, Triton paragraph: fp32 partials
+// plus a fused reduce/scale/cast kernel for M <= 64).  Here the whole thing
+// is one launch and needs no global scratch:
+//
+//   * swap-AB: the MMA's A operand is a 128-row tile of w (n on TMEM lanes),
+//     its B operand is all of x padded to MP rows (m on TMEM columns), so one
+//     tcgen05.mma 128 x MP x 32 covers every token at once;
+//   * each CTA of a thread-block cluster of `splits` CTAs owns one 128-row
+//     n-tile and a contiguous range of 128-byte K blocks, streamed through a
+//     TMA mbarrier ring (w with an L2 evict-first hint, x evict-last);
+//   * the fp32 partial accumulators are parked in each CTA's shared memory
+//     and summed across the cluster through distributed shared memory in a
+//     fixed order (split 0, 1, ...), then scaled, rounded to bf16 and stored.
+//
+// Roles: warps 0-3 load (one thread issues TMA; all four with `realign`) and
+// then act as the epilogue (warp w reads TMEM lanes 32w..32w+31); warp 4
+// allocates TMEM and issues the MMAs.  All waits are bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "realign.cuh"
+
+namespace fp8g {
+namespace {
+
+constexpr int kBN = 128;   // rows of w per tile (MMA M, TMEM lanes)
+constexpr int kBK = 128;   // bytes of K per stage
+constexpr int kMmaK = 32;
+constexpr int kMmaWarp = 4;
+constexpr int kThreads = 160;
+
+template <int MP>
+constexpr int tmem_cols_for() {
+  return MP <= 32 ? 32 : (MP <= 64 ? 64 : (MP <= 128 ? 128 : 256));
+}
+
+template <int MP, int STAGES, bool REALIGN>
+struct DCfg {
+  static constexpr int kABytes = kBN * kBK;
+  static constexpr int kBBytes = MP * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kPartBytes = kBN * MP * 4;
+  static constexpr int kDataBytes =
+      STAGES * kStageBytes > kPartBytes ? STAGES * kStageBytes : kPartBytes;
+  static constexpr int kBarOff = kDataBytes;
+  // full[S], empty[S], acc_full, mma_done, then tmem holder + abort flag
+  static constexpr int kNumBars = 2 * STAGES + 2;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  static constexpr int kTmemCols = tmem_cols_for<MP>();
+  static_assert(MP % 32 == 0 && MP >= 32 && MP <= 128, "MP");
+};
+
+__device__ __noinline__ bool drain_wait_d(uint32_t bar, uint32_t parity, unsigned* err,
+                                          uint64_t budget_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u && globaltimer_ns() - t0 > budget_ns) {
+      atomicOr(err, kErrWaitDrain);
+      return false;
+    }
+  }
+}
+
+template <int MP, int STAGES, bool REALIGN>
+__global__ void __launch_bounds__(kThreads)
+    fp8_linear_decode_kernel(const __grid_constant__ CUtensorMap tmW,
+                             const __grid_constant__ CUtensorMap tmX, const GemmArgs p,
+                             const int splits) {
+  using C = DCfg<MP, STAGES, REALIGN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+
+  const uint32_t bar0 = sbase + C::kBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_full_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t holder_addr = bar0 + 8u * C::kNumBars;
+  volatile uint32_t* holder =
+      reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOff + 8 * C::kNumBars);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(gbase + C::kBarOff + 8 * C::kNumBars + 4);
+  auto sA = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes); };
+  auto sB = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes + C::kABytes); };
+  const uint32_t part = sbase;  // fp32 partials [MP][128], reuses the ring after the mainloop
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int n_tile = static_cast<int>(blockIdx.x) / splits;
+  const int n0 = n_tile * kBN;
+  const int kb_begin = static_cast<int>((static_cast<long long>(p.num_kb) * rank) / splits);
+  const int kb_end = static_cast<int>((static_cast<long long>(p.num_kb) * (rank + 1)) / splits);
+  const int my_kb = kb_end - kb_begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), REALIGN ? 128u : 1u);
+      mbar_init(empty_bar(s), 1u);
+    }
+    mbar_init(acc_full_bar, 1u);
+    mbar_init(mma_done_bar, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(holder_addr, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (!REALIGN && threadIdx.x == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *holder;
+  const WaitCtx wc{p.err, abort_flag, p.budget_ns};
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ producer
+    if (!REALIGN) {
+      if (threadIdx.x == 0) {
+        const uint64_t pol_stream = l2_policy_evict_first();
+        const uint64_t pol_keep = l2_policy_evict_last();
+        uint32_t stage = 0, phase = 0, issued = 0;
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) break;
+          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          tma_load_2d_hint(sA(stage), &tmW, full_bar(stage), kb * kBK, n0, pol_stream);
+          tma_load_2d_hint(sB(stage), &tmX, full_bar(stage), kb * kBK, 0, pol_keep);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued > static_cast<uint32_t>(s)) {
+            const uint32_t n_s = (issued - 1u - s) / STAGES + 1u;
+            drain_wait_d(full_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      const int ptid = static_cast<int>(threadIdx.x);
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) break;
+        load_tile_realign<kBN, 128, 4>(sA(stage), p.w, p.N, p.K, n0, kb * kBK, ptid);
+        load_tile_realign<MP, 128, (MP * 8 / 128) >= 4 ? 4 : (MP * 8 / 128)>(
+            sB(stage), p.x, p.M, p.K, 0, kb * kBK, ptid);
+        fence_proxy_async_smem();
+        mbar_arrive(full_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ partials
+    // TMEM lane = n within the tile, column = m.  Park them in shared memory
+    // as part[m][n] so the cluster reduction reads 16-byte runs along n.
+    const bool have_acc = (my_kb == 0) || mbar_wait_bounded(acc_full_bar, 0u, wc, kErrWaitEpilogue);
+    if (have_acc) {
+      tc_fence_after_sync();
+      const uint32_t n_local = warp * 32u + lane;
+#pragma unroll 1
+      for (int c = 0; c < MP / 32; ++c) {
+        uint32_t v[32];
+        if (my_kb > 0) {
+          tmem_ld_32x32b_x32(tmem_base + ((warp * 32u) << 16) + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          sts_f32(part + static_cast<uint32_t>(((c * 32 + j) * kBN + n_local) * 4),
+                  __uint_as_float(v[j]));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_e4m3_f32(kBN, MP);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait_bounded(full_bar(stage), phase, wc, kErrWaitMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
+        const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
+#pragma unroll
+        for (int k = 0; k < kBK / kMmaK; ++k)
+          tc_mma_f8(tmem_base, a_desc + 2u * k, b_desc + 2u * k, kIdesc,
+                    (kb > kb_begin || k > 0) ? 1u : 0u);
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok && my_kb > 0) tc_commit(acc_full_bar);
+      tc_commit(mma_done_bar);
+      drain_wait_d(mma_done_bar, 0u, p.err, p.budget_ns);
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- reduce
+  // Every CTA of the cluster has parked its partials; each now reduces an
+  // equal share of the M x 128 outputs of this n-tile, reading all partials
+  // through distributed shared memory, and stores scaled bf16.
+  tc_fence_before_sync();
+  cluster_sync_all();
+  {
+    const int groups = p.M * (kBN / 4);  // float4 groups of valid rows
+    const int g_begin = static_cast<int>((static_cast<long long>(groups) * rank) / splits);
+    const int g_end = static_cast<int>((static_cast<long long>(groups) * (rank + 1)) / splits);
+    for (int g = g_begin + static_cast<int>(threadIdx.x); g < g_end; g += kThreads) {
+      const int m = g / (kBN / 4);
+      const int nl = (g % (kBN / 4)) * 4;
+      const uint32_t off = part + static_cast<uint32_t>((m * kBN + nl) * 4);
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < splits; ++q) {
+        const float4 v = ld_dsmem_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      const int n = n0 + nl;
+      uint16_t* yr = p.y + static_cast<size_t>(m) * static_cast<size_t>(p.N);
+      if (n + 4 <= p.N) {
+        const float4 sc = make_float4(__ldg(p.scale + n), __ldg(p.scale + n + 1),
+                                      __ldg(p.scale + n + 2), __ldg(p.scale + n + 3));
+        const uint32_t lo = pack_bf16x2(s.x * sc.x, s.y * sc.y);
+        const uint32_t hi = pack_bf16x2(s.z * sc.z, s.w * sc.w);
+        if (p.vec_store) {
+          *reinterpret_cast<uint2*>(yr + n) = make_uint2(lo, hi);
+        } else {
+          yr[n] = static_cast<uint16_t>(lo & 0xFFFFu);
+          yr[n + 1] = static_cast<uint16_t>(lo >> 16);
+          yr[n + 2] = static_cast<uint16_t>(hi & 0xFFFFu);
+          yr[n + 3] = static_cast<uint16_t>(hi >> 16);
+        }
+      } else {
+        const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (n + j < p.N) {
+            const uint32_t b = pack_bf16x2(sv[j] * __ldg(p.scale + n + j), 0.f);
+            yr[n + j] = static_cast<uint16_t>(b & 0xFFFFu);
+          }
+        }
+      }
+    }
+  }
+  // nobody leaves while another CTA may still read its shared memory
+  cluster_sync_all();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ dispatch
+struct DEntry {
+  int mp, stages;
+  bool realign;
+  const void* fn;
+  int smem;
+};
+
+template <int MP, int S, bool R>
+DEntry make_dentry() {
+  return DEntry{MP, S, R, reinterpret_cast<const void*>(&fp8_linear_decode_kernel<MP, S, R>),
+                DCfg<MP, S, R>::kSmemBytes};
+}
+
+const DEntry kDEntries[] = {
+    make_dentry<32, 2, false>(),  make_dentry<32, 3, false>(),  make_dentry<32, 4, false>(),
+    make_dentry<32, 6, false>(),  make_dentry<64, 2, false>(),  make_dentry<64, 3, false>(),
+    make_dentry<64, 4, false>(),  make_dentry<128, 2, false>(), make_dentry<128, 4, false>(),
+    make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),   make_dentry<64, 3, true>(),
+    make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
+};
+
+const DEntry* dfind(int mp, int stages, bool realign) {
+  for (const DEntry& e : kDEntries)
+    if (e.mp == mp && e.stages == stages && e.realign == realign) return &e;
+  return nullptr;
+}
+
+}  // namespace
+
+bool dec_config_supported(int mp, int stages, bool realign) {
+  return dfind(mp, stages, realign) != nullptr;
+}
+
+int dec_smem_bytes(int mp, int stages, bool realign) {
+  const DEntry* e = dfind(mp, stages, realign);
+  return e ? e->smem : -1;
+}
+
+int dec_threads(bool) { return kThreads; }
+
+int dec_tmem_cols(int mp) { return mp <= 32 ? 32 : (mp <= 64 ? 64 : (mp <= 128 ? 128 : 256)); }
+
+cudaError_t dec_prepare(int mp, int stages, bool realign) {
+  const DEntry* e = dfind(mp, stages, realign);
+  if (!e) return cudaErrorInvalidValue;
+  cudaError_t r =
+      cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
+  if (r != cudaSuccess) return r;
+  return cudaSuccess;
+}
+
+cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out) {
+  const DEntry* e = dfind(mp, stages, realign);
+  if (!e) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, e->fn, kThreads,
+                                                       static_cast<size_t>(e->smem));
+}
+
+cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,
+                                    int* out) {
+  const DEntry* e = dfind(mp, stages, realign);
+  if (!e) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, e->fn, &cfg);
+}
+
+cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                          const DecConfig& c, cudaStream_t s) {
+  const DEntry* e = dfind(c.mp, c.stages, c.realign);
+  if (!e) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c.n_tiles * c.splits));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  CUtensorMap mA = tmA, mB = tmB;
+  GemmArgs args = a;
+  int splits = c.splits;
+  void* params[] = {&mA, &mB, &args, &splits};
+  return cudaLaunchKernelExC(&cfg, e->fn, params);
+}
+
+}  // namespace fp8g

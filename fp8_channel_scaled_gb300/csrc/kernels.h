@@ -1,0 +1,61 @@
+// kernels.h -- internal interface between the C-ABI host code (api.cu) and
+// the kernel translation units.  Not part of the public API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8g {
+
+// Operands and bookkeeping shared by every GEMM kernel.
+struct GemmArgs {
+  const uint8_t* x;      // E4M3 [M, K] row-major
+  const uint8_t* w;      // E4M3 [N, K] row-major
+  const float* scale;    // fp32 [N]
+  uint16_t* y;           // bf16 [M, N] row-major
+  int M, N, K;
+  int num_kb;            // ceil(K / 128)
+  int vec_store;         // 1: y rows are 16-byte aligned (N % 8 == 0, y aligned)
+  unsigned* err;         // device error word
+  unsigned long long budget_ns;  // longest single wait before giving up
+};
+
+// ---- persistent tcgen05 kernel (large M) ---------------------------------
+struct TcConfig {
+  int bn;          // N tile (128 or 256); the M tile is 128, the K block 128 bytes
+  int stages;      // shared-memory pipeline depth
+  bool realign;    // operands loaded by the realigning producer instead of TMA
+  int grid;        // persistent CTAs
+  int group_m;     // M tiles per raster group
+};
+bool tc_config_supported(int bn, int stages, bool realign);
+int tc_smem_bytes(int bn, int stages, bool realign);
+int tc_threads(bool realign);
+int tc_max_stages(int bn, bool realign, int smem_optin);
+cudaError_t tc_prepare(int bn, int stages, bool realign);  // per device, before first launch
+cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                      const TcConfig& c, cudaStream_t s);
+
+// ---- split-K decode kernel (small M, swap-AB, cluster reduce) -------------
+struct DecConfig {
+  int mp;          // M padded to the MMA N dimension (32, 64 or 128)
+  int stages;      // shared-memory pipeline depth
+  bool realign;    // operands loaded by the realigning producer instead of TMA
+  int splits;      // K splits = cluster size (1..8)
+  int n_tiles;     // ceil(N / 128)
+};
+bool dec_config_supported(int mp, int stages, bool realign);
+int dec_smem_bytes(int mp, int stages, bool realign);
+int dec_threads(bool realign);
+int dec_tmem_cols(int mp);
+cudaError_t dec_prepare(int mp, int stages, bool realign);
+cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out);
+cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,
+                                    int* out);
+cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                          const DecConfig& c, cudaStream_t s);
+
+
+}  // namespace fp8g

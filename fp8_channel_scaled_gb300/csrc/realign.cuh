@@ -1,0 +1,106 @@
+// realign.cuh -- operand loader for rows that are not 16-byte aligned.
+//
+// A TMA tensor map needs every row pitch to be a multiple of 16 bytes, so a
+// row-major E4M3 matrix with K % 16 != 0 (e.g. K = 4127) cannot be tiled by
+// TMA.  Instead of padding a copy on the host or in a separate pass (what
+// the pages' submissions do for K = 4127: "Kimi K3 (256k)" page, SM100
+// tcgen05 paragraph; "claude-fable-5" page, SM120 funnel-shift pad-copy
+// paragraph), producer threads read each row segment with 16-byte aligned
+// loads, shift the bytes into place in registers, zero everything at
+// k >= K, and write the result straight into the 128-byte-swizzled K-major
+// shared-memory layout the tensor cores read.  Zero bytes contribute exactly
+// nothing to the dot product, so the result equals the unpadded one.
+//
+// Every global load touches a 16-byte word that contains at least one byte
+// of the requested row segment, so no load leaves the operand's own
+// 16-byte-aligned granules.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace fp8g {
+
+// Bytes [sh, sh+16) of the 32-byte little-endian value hi:lo.
+__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uint32_t sh) {
+  const uint32_t u0 = lo.x, u1 = lo.y, u2 = lo.z, u3 = lo.w;
+  const uint32_t u4 = hi.x, u5 = hi.y, u6 = hi.z, u7 = hi.w;
+  const uint32_t q = sh >> 2;
+  const uint32_t bits = (sh & 3u) * 8u;
+  uint32_t t0, t1, t2, t3, t4;
+  if (q == 0) {
+    t0 = u0; t1 = u1; t2 = u2; t3 = u3; t4 = u4;
+  } else if (q == 1) {
+    t0 = u1; t1 = u2; t2 = u3; t3 = u4; t4 = u5;
+  } else if (q == 2) {
+    t0 = u2; t1 = u3; t2 = u4; t3 = u5; t4 = u6;
+  } else {
+    t0 = u3; t1 = u4; t2 = u5; t3 = u6; t4 = u7;
+  }
+  uint4 r;
+  r.x = __funnelshift_r(t0, t1, bits);
+  r.y = __funnelshift_r(t1, t2, bits);
+  r.z = __funnelshift_r(t2, t3, bits);
+  r.w = __funnelshift_r(t3, t4, bits);
+  return r;
+}
+
+// Keep the first `valid` bytes (0..16) of v, zero the rest.
+__device__ __forceinline__ uint4 keep_bytes(uint4 v, int valid) {
+  auto m = [](int nb) -> uint32_t {
+    return nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : ((1u << (8 * nb)) - 1u));
+  };
+  v.x &= m(valid);
+  v.y &= m(valid - 4);
+  v.z &= m(valid - 8);
+  v.w &= m(valid - 12);
+  return v;
+}
+
+// Copy rows [r0, r0+R) x bytes [k0, k0+128) of a row-major byte matrix with
+// `rows_total` rows and pitch K bytes into the K-major 128-byte-swizzled
+// tile at shared address `dst` (1024-byte aligned): row r's 16-byte chunk c
+// lands at r*128 + ((c ^ (r & 7)) * 16).  Rows >= rows_total and bytes at
+// k >= K are written as zeros.  NT threads (tid in [0, NT)) share the work;
+// consecutive threads take consecutive chunks of a row, so loads coalesce.
+template <int R, int NT, int BATCH>
+__device__ __forceinline__ void load_tile_realign(uint32_t dst, const uint8_t* __restrict__ src,
+                                                  int rows_total, int K, int r0, int k0,
+                                                  int tid) {
+  constexpr int UNITS = R * 8;
+  static_assert(UNITS % NT == 0, "units must split evenly");
+  constexpr int PER = UNITS / NT;
+  static_assert(PER % BATCH == 0, "batch must divide the per-thread units");
+#pragma unroll
+  for (int b = 0; b < PER; b += BATCH) {
+    uint4 lo[BATCH], hi[BATCH];
+    uint32_t sh[BATCH];
+    int valid[BATCH];
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int u = (b + i) * NT + tid;
+      const int r = u >> 3, c = u & 7;
+      const int grow = r0 + r, kc = k0 + 16 * c;
+      lo[i] = make_uint4(0, 0, 0, 0);
+      hi[i] = make_uint4(0, 0, 0, 0);
+      sh[i] = 0;
+      valid[i] = 0;
+      if (grow < rows_total && kc < K) {
+        valid[i] = min(16, K - kc);
+        const uint8_t* p = src + static_cast<size_t>(grow) * static_cast<size_t>(K) + kc;
+        sh[i] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p) & 15u);
+        const uint8_t* base = p - sh[i];
+        lo[i] = ldg_nc_v4(base);
+        if (sh[i] != 0u && valid[i] > 16 - static_cast<int>(sh[i])) hi[i] = ldg_nc_v4(base + 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int u = (b + i) * NT + tid;
+      const int r = u >> 3, c = u & 7;
+      uint4 v = keep_bytes(realign16(lo[i], hi[i], sh[i]), valid[i]);
+      sts_v4(dst + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)), v);
+    }
+  }
+}
+
+}  // namespace fp8g

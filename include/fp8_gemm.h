@@ -1,0 +1,163 @@
+/*
+ * fp8_gemm.h -- C ABI of the GB300 (sm_103a) per-output-channel scaled FP8
+ * linear layer.
+ *
+ *     y[m, n] = bf16_rn( (sum_k x[m, k] * w[n, k], accumulated in fp32)
+ *                        * weight_scale[n] )
+ *
+ * The operation is the FP8 GEMM audited on the kernelbench.com model pages:
+ * E4M3 operands with fp32 accumulation ("Kimi K3 (256k)" page, SM120 FP8 GEMM
+ * paragraph; "deepseek-v4-flash" page, CUTLASS SM90 paragraph), the live
+ * per-output-channel weight_scale applied to the accumulator in the epilogue
+ * and a bf16 result ("Kimi K3 (256k)" page, SM90 WGMMA and sm_100 tcgen05
+ * paragraphs; "claude-fable-5" page, CUTLASS 4.0 SM100 paragraph), over the
+ * problem's large-M, M = 32 decode and K = 4127 shapes.
+ *
+ * Conventions shared by every entry point:
+ *   - Status: every function returns an fp8gemm_status (0 = OK).  No
+ *     exception or signal crosses the ABI.
+ *   - Streams: `stream` is a CUDA runtime stream handle (cudaStream_t); NULL
+ *     means the legacy default stream.  Compute calls are asynchronous with
+ *     respect to the host and never synchronise.
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     device memory per call; it keeps, per device, only its properties and
+ *     a 4-byte device error word (see fp8_gemm_check_device_error).
+ *   - Nothing derived from the data is ever cached: each call reads x, w
+ *     and weight_scale as they are when the kernel runs (the pages' stale
+ *     padded-input failure, "qwen3.8-max" page, odd-K pad-cache paragraph,
+ *     is impossible by construction).
+ *   - Thread safety: calls may come from several host threads.
+ */
+#ifndef FP8_GEMM_H
+#define FP8_GEMM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA runtime stream handle without including CUDA headers
+ * (identical to cudaStream_t). */
+typedef struct CUstream_st *fp8gemm_stream_t;
+
+#define FP8GEMM_VERSION 1
+
+typedef enum {
+    FP8GEMM_OK = 0,
+    FP8GEMM_EINVAL = 1,    /* null pointer, bad size, host pointer, aliasing y */
+    FP8GEMM_EALIGN = 2,    /* weight_scale not 4-byte or y not 2-byte aligned */
+    FP8GEMM_EDEVICE = 3,   /* no CUDA device, or not compute capability 10.3 */
+    FP8GEMM_ELAUNCH = 4,   /* the CUDA launch (or a CUDA runtime call) failed */
+    FP8GEMM_ETIMEOUT = 5,  /* a kernel gave up a bounded wait (results invalid) */
+    FP8GEMM_EUNSUPPORTED = 6 /* the options ask for a configuration not built */
+} fp8gemm_status;
+
+/* Kernel path. */
+enum {
+    FP8GEMM_PATH_AUTO = 0,    /* M <= 64: decode path, else main path */
+    FP8GEMM_PATH_MAIN = 1,    /* persistent tcgen05 tile kernel */
+    FP8GEMM_PATH_DECODE = 2   /* split-K swap-AB kernel; needs M <= 128 */
+};
+
+/*
+ * Optional tuning and test knobs; a zero-initialised struct (or NULL)
+ * means "choose automatically".
+ */
+typedef struct {
+    int path;           /* FP8GEMM_PATH_* */
+    int force_realign;  /* 1: load operands with the realigning producer even
+                           when TMA could (tests the K % 16 != 0 loader) */
+    int tile_n;         /* main path N tile: 0 auto, 128 or 256 */
+    int stages;         /* pipeline depth: 0 auto */
+    int splits;         /* decode path K splits (cluster size): 0 auto, 1..8 */
+    int reserved[3];    /* must be zero */
+} fp8gemm_options;
+
+/* What a call with the same arguments would launch (see fp8_gemm_plan). */
+typedef struct {
+    int path;           /* FP8GEMM_PATH_MAIN or FP8GEMM_PATH_DECODE; 0 = no launch */
+    int realign;        /* 1: operands loaded by the realigning producer */
+    int tile_m;         /* rows of x per tile (main) / rows of w per tile (decode) */
+    int tile_n;         /* columns of y per tile (main) / padded M (decode) */
+    int stages;         /* shared-memory pipeline depth */
+    int splits;         /* K splits (decode), 1 for main */
+    int grid;           /* CTAs launched */
+    int cluster;        /* CTAs per cluster */
+    int threads;        /* threads per CTA */
+    int smem_bytes;     /* dynamic shared memory per CTA */
+    int launches;       /* kernels launched by one call (0 or 1) */
+} fp8gemm_plan;
+
+/*
+ * fp8_gemm_scaled -- y = bf16((x . w^T, fp32 acc) * weight_scale), on `stream`.
+ *
+ *   x      device, E4M3FN bytes, [M, K] row-major (K contiguous), any alignment
+ *   w      device, E4M3FN bytes, [N, K] row-major (nn.Linear layout), any alignment
+ *   scale  device, fp32 [N], 4-byte aligned
+ *   y      device, bf16 [M, N] row-major, 2-byte aligned; written, never read.
+ *          Must not overlap x, w or scale.
+ *   M,N,K  >= 0.  M == 0 or N == 0: nothing is launched.  K == 0: y = 0.
+ *
+ * Rows whose pitch K is not a multiple of 16 bytes (e.g. K = 4127), or
+ * operands not 16-byte aligned, are loaded by an in-kernel realigning
+ * producer; bytes past K are treated as zeros, which adds exactly nothing
+ * (the zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
+ * paragraph).  No padded copy is made.
+ *
+ * Returns FP8GEMM_OK once the kernel is enqueued.  Errors inside the kernel
+ * (a bounded wait that ran out) are reported by fp8_gemm_check_device_error.
+ */
+int fp8_gemm_scaled(const void *x, const void *w, const float *scale, void *y,
+                    int M, int N, int K, fp8gemm_stream_t stream);
+
+/* As fp8_gemm_scaled, with options (NULL = automatic). */
+int fp8_gemm_scaled_ex(const void *x, const void *w, const float *scale, void *y,
+                       int M, int N, int K, const fp8gemm_options *opt,
+                       fp8gemm_stream_t stream);
+
+/*
+ * fp8_gemm_plan -- fill *out with what fp8_gemm_scaled_ex would launch for
+ * these sizes on CUDA device `device`, without launching anything.  x and w
+ * are used only for their alignment and may be NULL (taken as 16-byte
+ * aligned).
+ */
+int fp8_gemm_plan(int device, const void *x, const void *w, int M, int N, int K,
+                  const fp8gemm_options *opt, fp8gemm_plan *out);
+
+/*
+ * fp8_gemm_check_device_error -- synchronise `stream`, read and clear the
+ * device error word of the current device.  FP8GEMM_ETIMEOUT means some
+ * kernel launched since the last check gave up a bounded wait and its output
+ * is invalid; FP8GEMM_ELAUNCH means the stream reported a CUDA error.
+ */
+int fp8_gemm_check_device_error(fp8gemm_stream_t stream);
+
+/* Raw value of the device error word as last read by
+ * fp8_gemm_check_device_error (bit flags; 0 = none). */
+unsigned fp8_gemm_last_device_error_bits(void);
+
+/* Longest single wait inside a kernel, in nanoseconds (default 1e9, or the
+ * FP8GEMM_WAIT_BUDGET_NS environment variable at load).  0 restores the
+ * default.  Applies to launches made after the call. */
+int fp8_gemm_set_wait_budget_ns(unsigned long long ns);
+
+/*
+ * fp8_gemm_selftest_wait_timeout -- launch one tiny kernel whose single
+ * thread waits on an mbarrier that nothing ever completes, with the given
+ * budget (ns).  The wait must run out, record its error bit and return, so
+ * that fp8_gemm_check_device_error then reports FP8GEMM_ETIMEOUT and the
+ * context stays usable.  Exercises the bounded-wait machinery every kernel
+ * relies on, without faulting or hanging the GPU.
+ */
+int fp8_gemm_selftest_wait_timeout(unsigned long long budget_ns, fp8gemm_stream_t stream);
+
+/* Static description of a status code. */
+const char *fp8_gemm_status_string(int status);
+
+/* FP8GEMM_VERSION of the built library. */
+int fp8_gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8_GEMM_H */

@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Every comparison is element by element on the same seeded inputs, within
+|dy| <= 2^-7 |y_ref| + 1e-3; the exactness pins (one-hot weights, small
+integer operands, zero K padding, TMA vs realigning loader) are bitwise.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import compare, to_dev, y_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import fp8_channel_scaled_gb300 as fg  # noqa: E402
+from fp8_channel_scaled_gb300 import Options, PATH_DECODE, PATH_MAIN  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from fp8_channel_scaled_gb300 import build
+    build.build()
+    fg.lib()
+    yield
+    assert fg.fp8_gemm_check_device_error() == 0
+
+
+def run(x, w, s, options=None, y=None):
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    if y is None:
+        y = torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device="cuda")
+    if options is None:
+        fg.fp8_gemm_scaled(xd, wd, sd, y)
+    else:
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, options)
+    fg.check_device_error()
+    return y_bits(y)
+
+
+def check_full(x, w, s, options=None, what=""):
+    got = run(x, w, s, options)
+    ref = oracle.linear(x, w, s)
+    return compare(got, ref, what)
+
+
+# ------------------------------------------------------------------ small workload
+def test_small_workload_full():
+    x, w, s = synth.workload_inputs("small")
+    p = fg.plan(*x.shape[:1], w.shape[0], x.shape[1])
+    assert p.path == PATH_DECODE and p.launches == 1
+    check_full(x, w, s, what="small")
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_small_workload_both_paths(path):
+    x, w, s = synth.workload_inputs("small")
+    check_full(x, w, s, Options(path=path), what=f"small path {path}")
+
+
+# ------------------------------------------------------------------ main path shapes and tails
+MAIN_SHAPES = [
+    (128, 256, 128), (256, 512, 1024), (129, 136, 256), (200, 300, 520), (65, 8, 16),
+    (384, 264, 4127 // 8), (300, 257, 17), (130, 129, 129), (1, 1, 1), (77, 1000, 33),
+    (640, 1280, 4096),
+]
+
+
+@pytest.mark.parametrize("M,N,K", MAIN_SHAPES)
+def test_main_path_shapes(M, N, K):
+    x, w, s = synth.make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
+    check_full(x, w, s, Options(path=PATH_MAIN), what=f"main {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("realign", [False, True])
+def test_main_path_tiles_and_loaders(bn, realign):
+    x, w, s = synth.make_inputs(300, 520, 640, seed=5)
+    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn, force_realign=realign),
+               what=f"main bn={bn} realign={realign}")
+
+
+# ------------------------------------------------------------------ decode path shapes and tails
+DECODE_SHAPES = [
+    (1, 128, 128), (5, 136, 256), (32, 1024, 2048), (33, 1000, 1000), (64, 384, 4096),
+    (17, 257, 4127), (32, 128, 8192), (100, 256, 512), (2, 8, 16),
+]
+
+
+@pytest.mark.parametrize("M,N,K", DECODE_SHAPES)
+def test_decode_path_shapes(M, N, K):
+    x, w, s = synth.make_inputs(M, N, K, seed=M + N + K)
+    check_full(x, w, s, Options(path=PATH_DECODE), what=f"decode {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+def test_decode_splits(splits):
+    x, w, s = synth.make_inputs(32, 640, 2048, seed=splits)
+    check_full(x, w, s, Options(path=PATH_DECODE, splits=splits), what=f"splits {splits}")
+
+
+@pytest.mark.parametrize("M", [8, 40, 128])
+def test_decode_realign(M):
+    x, w, s = synth.make_inputs(M, 384, 1040, seed=M)
+    check_full(x, w, s, Options(path=PATH_DECODE, force_realign=True), what=f"decode realign M={M}")
+
+
+# ------------------------------------------------------------------ bitwise pins
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_one_hot_weights_reproduce_x_bitwise(path):
+    M = 64 if path == PATH_DECODE else 192
+    K = 256
+    x, _, _ = synth.make_inputs(M, 8, K, seed=21)
+    w = np.zeros((K, K), np.uint8)
+    w[np.arange(K), np.arange(K)] = 0x38  # 1.0
+    s = np.ones(K, np.float32)
+    got = run(x, w, s, Options(path=path))
+    ref = oracle.linear(x, w, s)
+    g, r = oracle.bf16_bits_to_f64(got), oracle.bf16_bits_to_f64(ref)
+    assert np.array_equal(g, r)
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_small_integer_operands_bitwise(path):
+    # E4M3 codes of the integers -16..16; every partial sum stays an integer
+    # below 2^24, so fp32 accumulation is exact and the only rounding is the
+    # final bf16 one, which both sides take once.
+    ints = np.arange(-16, 17, dtype=np.float64)
+    codes = synth.quantize_e4m3(ints)
+    rng = np.random.default_rng(7)
+    M = 48 if path == PATH_DECODE else 160
+    N, K = 272, 2048
+    x = rng.choice(codes, (M, K)).astype(np.uint8)
+    w = rng.choice(codes, (N, K)).astype(np.uint8)
+    s = (2.0 ** -rng.integers(0, 12, N)).astype(np.float32)
+    got = run(x, w, s, Options(path=path))
+    ref = oracle.linear(x, w, s)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_k_tail_equals_zero_padded_bitwise(path):
+    M = 40 if path == PATH_DECODE else 256
+    N, K, Kp = 384, 4127, 4224
+    x, w, s = synth.make_inputs(M, N, K, seed=31)
+    xp = np.zeros((M, Kp), np.uint8)
+    wp = np.zeros((N, Kp), np.uint8)
+    xp[:, :K], wp[:, :K] = x, w
+    a = run(x, w, s, Options(path=path))
+    b = run(xp, wp, s, Options(path=path))
+    assert np.array_equal(a, b)
+    compare(a, oracle.linear(x, w, s), "K=4127")
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_realign_loader_equals_tma_bitwise(path):
+    M = 64 if path == PATH_DECODE else 256
+    x, w, s = synth.make_inputs(M, 512, 1024, seed=41)
+    a = run(x, w, s, Options(path=path))
+    b = run(x, w, s, Options(path=path, force_realign=True))
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ unaligned and poisoned operands
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+@pytest.mark.parametrize("offset", [1, 5, 15])
+def test_unaligned_operand_bases_and_poisoned_neighbours(path, offset):
+    """x and w start at odd byte offsets inside larger buffers whose other
+    bytes are NaN codes; nothing outside [M,K] / [N,K] may leak into y."""
+    M = 24 if path == PATH_DECODE else 136
+    N, K = 264, 200
+    x, w, s = synth.make_inputs(M, N, K, seed=offset)
+    bx = torch.full((M * K + 64,), 0x7F, dtype=torch.uint8, device="cuda")
+    bw = torch.full((N * K + 64,), 0xFF, dtype=torch.uint8, device="cuda")
+    xd = bx[offset:offset + M * K].view(M, K)
+    wd = bw[offset:offset + N * K].view(N, K)
+    xd.copy_(to_dev(x))
+    wd.copy_(to_dev(w))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    p = fg.plan(M, N, K, Options(path=path), x=xd, w=wd)
+    assert p.realign == 1
+    fg.fp8_gemm_scaled_ex(xd, wd, to_dev(s), y, Options(path=path))
+    fg.check_device_error()
+    compare(y_bits(y), oracle.linear(x, w, s), f"offset {offset}")
+
+
+def test_output_guard_bands_untouched():
+    M, N, K = 130, 264, 384
+    x, w, s = synth.make_inputs(M, N, K, seed=3)
+    for path in (PATH_MAIN, PATH_DECODE):
+        Mp = M if path == PATH_MAIN else 50
+        buf = torch.full((Mp * N + 2 * 512,), -12345, dtype=torch.int16, device="cuda")
+        y = buf[512:512 + Mp * N].view(torch.bfloat16).view(Mp, N)
+        fg.fp8_gemm_scaled_ex(to_dev(x[:Mp]), to_dev(w), to_dev(s), y, Options(path=path))
+        fg.check_device_error()
+        host = buf.cpu().numpy()
+        assert np.all(host[:512] == -12345) and np.all(host[512 + Mp * N:] == -12345)
+        compare(y_bits(y), oracle.linear(x[:Mp], w, s), f"guard path {path}")
+
+
+def test_odd_n_scalar_store_path():
+    # N % 8 != 0 forces the element-wise store path; y base misaligned to 2 bytes
+    M, N, K = 140, 131, 256
+    x, w, s = synth.make_inputs(M, N, K, seed=8)
+    buf = torch.empty(M * N + 1, dtype=torch.bfloat16, device="cuda")
+    y = buf[1:].view(M, N)
+    fg.fp8_gemm_scaled_ex(to_dev(x), to_dev(w), to_dev(s), y, Options(path=PATH_MAIN))
+    fg.check_device_error()
+    compare(y_bits(y), oracle.linear(x, w, s), "odd N")
+
+
+# ------------------------------------------------------------------ degenerate sizes
+def test_empty_and_k_zero():
+    s = to_dev(np.ones(16, np.float32))
+    y = torch.full((4, 16), 7.0, dtype=torch.bfloat16, device="cuda")
+    x0 = torch.empty((4, 0), dtype=torch.uint8, device="cuda")
+    w0 = torch.empty((16, 0), dtype=torch.uint8, device="cuda")
+    for path in (PATH_MAIN, PATH_DECODE):
+        y.fill_(7.0)
+        fg.fp8_gemm_scaled_ex(x0, w0, s, y, Options(path=path))
+        fg.check_device_error()
+        assert torch.all(y == 0)
+    # M == 0: nothing launched, nothing written
+    ye = torch.empty((0, 16), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_scaled(torch.empty((0, 8), dtype=torch.uint8, device="cuda"),
+                       torch.zeros((16, 8), dtype=torch.uint8, device="cuda"), s, ye)
+
+
+# ------------------------------------------------------------------ stress protocol of the pages
+def test_in_place_rescale_and_same_buffer_recompute():
+    """Weights and scales rescaled in place, and x overwritten in place with
+    the same pointer: every call recomputes from the live contents."""
+    for path, M in ((PATH_MAIN, 256), (PATH_DECODE, 32)):
+        N, K = 512, 4127
+        x, w, s = synth.make_inputs(M, N, K, seed=51)
+        xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(path=path))
+        fg.check_device_error()
+        compare(y_bits(y), oracle.linear(x, w, s), "first")
+        s2 = (s * np.float32(3.0)).astype(np.float32)
+        sd.copy_(to_dev(s2))
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(path=path))
+        fg.check_device_error()
+        compare(y_bits(y), oracle.linear(x, w, s2), "rescaled scale")
+        x2, w2, _ = synth.make_inputs(M, N, K, seed=52)
+        x2[0, :] = x[0, :]  # change everything except one row
+        xd.copy_(to_dev(x2))
+        wd.copy_(to_dev(w2))
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(path=path))
+        fg.check_device_error()
+        compare(y_bits(y), oracle.linear(x2, w2, s2), "new x, w in place")
+
+
+# ------------------------------------------------------------------ errors and bounded waits
+def test_bounded_wait_times_out_and_context_survives():
+    fg.fp8_gemm_selftest_wait_timeout(2_000_000)  # 2 ms
+    assert fg.fp8_gemm_check_device_error() == 5
+    assert fg.lib().fp8_gemm_last_device_error_bits() & (1 << 4)
+    assert fg.fp8_gemm_check_device_error() == 0  # cleared
+    x, w, s = synth.workload_inputs("small")
+    check_full(x, w, s, what="after timeout")
+
+
+def test_rejects_host_pointers_and_aliasing():
+    x = torch.zeros((4, 32), dtype=torch.uint8)
+    w = torch.zeros((8, 32), dtype=torch.uint8, device="cuda")
+    s = torch.ones(8, dtype=torch.float32, device="cuda")
+    y = torch.empty((4, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled(x, w, s, y)
+    assert e.value.status == 1
+    buf = torch.zeros(4 * 32 + 64, dtype=torch.uint8, device="cuda")
+    xa = buf[:128].view(4, 32)
+    ya = buf[64:128].view(torch.bfloat16).view(4, 8)
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled(xa, w, s, ya)
+    assert e.value.status == 1
+    assert fg.fp8_gemm_check_device_error() == 0
