@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     fp8_gemm_set_wait_budget_ns,
     fp8_gemm_status_string,
     fp8_gemm_version,
+    fp8_gemm_workspace_bytes,
     lib,
     library_path,
     linear,

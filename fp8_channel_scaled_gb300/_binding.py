@@ -24,13 +24,17 @@ class FP8GemmError(RuntimeError):
 class _COptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("force_realign", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("splits", ctypes.c_int),
-                ("reserved", ctypes.c_int * 3)]
+                ("no_workspace", ctypes.c_int), ("reserved", ctypes.c_int * 2),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
+                    "threads", "smem_bytes", "launches", "repitch", "occupancy")
 
 
 class _CPlan(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in (
-        "path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
-        "threads", "smem_bytes", "launches")]
+    _fields_ = [(n, ctypes.c_int) for n in _PLAN_INT_FIELDS] + [
+        ("workspace_bytes", ctypes.c_size_t)]
 
 
 @dataclass
@@ -40,11 +44,17 @@ class Options:
     tile_n: int = 0
     stages: int = 0
     splits: int = 0
+    no_workspace: bool = False
+    workspace: int = 0          # device pointer (e.g. tensor.data_ptr()), 0 = library pool
+    workspace_bytes: int = 0
 
     def _c(self) -> _COptions:
         o = _COptions()
         o.path, o.force_realign = int(self.path), int(bool(self.force_realign))
         o.tile_n, o.stages, o.splits = int(self.tile_n), int(self.stages), int(self.splits)
+        o.no_workspace = int(bool(self.no_workspace))
+        o.workspace = int(self.workspace) or None
+        o.workspace_bytes = int(self.workspace_bytes)
         return o
 
 
@@ -61,6 +71,9 @@ class Plan:
     threads: int
     smem_bytes: int
     launches: int
+    repitch: int
+    occupancy: int
+    workspace_bytes: int
 
 
 _lock = threading.RLock()
@@ -86,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_scaled_ex.argtypes = [vp, vp, vp, vp, i, i, i, ctypes.POINTER(_COptions), st]
         L.fp8_gemm_plan.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions),
                                     ctypes.POINTER(_CPlan)]
+        L.fp8_gemm_workspace_bytes.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions)]
+        L.fp8_gemm_workspace_bytes.restype = ctypes.c_size_t
         L.fp8_gemm_check_device_error.argtypes = [st]
         L.fp8_gemm_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
         L.fp8_gemm_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, st]
@@ -163,7 +178,14 @@ def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None =
     p = _CPlan()
     _check(lib().fp8_gemm_plan(int(device), x_ptr or None, w_ptr or None, int(M), int(N), int(K),
                                ctypes.byref(o), ctypes.byref(p)), "fp8_gemm_plan")
-    return Plan(*[getattr(p, f[0]) for f in _CPlan._fields_])
+    return Plan(*[getattr(p, f) for f in _PLAN_INT_FIELDS], int(p.workspace_bytes))
+
+
+def fp8_gemm_workspace_bytes(device: int, M: int, N: int, K: int, options: Options | None = None,
+                             x_ptr: int = 0, w_ptr: int = 0) -> int:
+    o = (options or Options())._c()
+    return int(lib().fp8_gemm_workspace_bytes(int(device), x_ptr or None, w_ptr or None, int(M),
+                                              int(N), int(K), ctypes.byref(o)))
 
 
 def fp8_gemm_check_device_error(stream=None) -> int:

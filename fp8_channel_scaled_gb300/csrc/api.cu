@@ -6,8 +6,9 @@
 // "claude-fable-5" page, Triton paragraph: split-K for M <= 64): M <= 64
 // takes the split-K decode kernel, everything else the persistent tile
 // kernel.  Rows that TMA cannot describe (pitch not a multiple of 16 bytes,
-// or a base not 16-byte aligned) switch either kernel to its realigning
-// producer.  Nothing derived from operand data is cached.
+// or a base not 16-byte aligned) are first repitched into a workspace on the
+// main path, or loaded by the in-kernel realigning producer on the decode
+// path.  Nothing derived from operand data is cached.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,6 +51,7 @@ struct DevState {
   int sm_count = 0;
   int smem_optin = 0;
   unsigned* err_word = nullptr;
+  cudaMemPool_t pool = nullptr;  // private stream-ordered pool for repitch workspaces
 };
 
 std::mutex g_mu;
@@ -75,15 +77,19 @@ unsigned long long budget_ns() {
   return g_budget_ns;
 }
 
-// Per-device set-up, once: properties, error word address, kernel attributes.
+const int kTcTiles[] = {256, 224, 192, 160, 128};
+const int kTcStages[] = {3, 4, 5, 6, 7};
+const int kDecMp[] = {32, 64, 128};
+const int kDecStages[] = {2, 3, 4, 6};
+
+// Per-device set-up, once: properties, error word address, kernel attributes,
+// workspace pool.
 int device_state(int dev, DevState** out) {
   if (dev < 0 || dev >= kMaxDevices) return FP8GEMM_EDEVICE;
   std::lock_guard<std::mutex> lk(g_mu);
   DevState& d = g_dev[dev];
-  if (d.init) {
-    *out = &d;
-    return d.status;
-  }
+  *out = &d;
+  if (d.init) return d.status;
   d.init = true;
   d.status = FP8GEMM_EDEVICE;
   int major = 0, minor = 0;
@@ -94,18 +100,13 @@ int device_state(int dev, DevState** out) {
       cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
           cudaSuccess) {
     cudaGetLastError();
-    *out = &d;
     return d.status;
   }
-  if (major != 10 || minor != 3) {  // the library is built for sm_103a only
-    *out = &d;
-    return d.status;
-  }
+  if (major != 10 || minor != 3) return d.status;  // the library is built for sm_103a only
   d.status = FP8GEMM_ELAUNCH;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err_word), g_device_error_word) !=
       cudaSuccess) {
     cudaGetLastError();
-    *out = &d;
     return d.status;
   }
   if (!g_encode) {
@@ -115,31 +116,37 @@ int device_state(int dev, DevState** out) {
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn) {
       cudaGetLastError();
-      *out = &d;
       return d.status;
     }
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
-  const int bns[] = {128, 256};
-  const int tc_stages[] = {3, 4, 6};
   for (bool r : {false, true}) {
-    for (int bn : bns)
-      for (int s : tc_stages)
+    for (int bn : kTcTiles)
+      for (int s : kTcStages)
         if (tc_config_supported(bn, s, r) && tc_prepare(bn, s, r) != cudaSuccess) {
           cudaGetLastError();
-          *out = &d;
           return d.status;
         }
-    for (int mp : {32, 64, 128})
-      for (int s : {2, 3, 4, 6})
+    for (int mp : kDecMp)
+      for (int s : kDecStages)
         if (dec_config_supported(mp, s, r) && dec_prepare(mp, s, r) != cudaSuccess) {
           cudaGetLastError();
-          *out = &d;
           return d.status;
         }
   }
+  cudaMemPoolProps props;
+  std::memset(&props, 0, sizeof(props));
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  if (cudaMemPoolCreate(&d.pool, &props) == cudaSuccess) {
+    uint64_t keep = ~0ull;  // keep freed workspace memory for the next call
+    cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  } else {
+    cudaGetLastError();
+    d.pool = nullptr;  // calls then fall back to the realigning producer
+  }
   d.status = FP8GEMM_OK;
-  *out = &d;
   return d.status;
 }
 
@@ -161,9 +168,12 @@ struct Plan {
   fp8gemm_plan pub;
   TcConfig tc;
   DecConfig dec;
+  int Kp;               // row pitch of the repitched operands
+  size_t x_off, w_off;  // offsets of the repitched x and w inside the workspace
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
 
 // Resident decode CTAs per SM, or 0 if the configuration cannot run.  The
 // tensor-memory budget (512 columns per SM) must cover every resident CTA, or
@@ -180,59 +190,100 @@ int dec_occupancy(const DevState& d, int mp, int stages, bool realign) {
   return blocks;
 }
 
+// Main path tile choice: the N tile (with the deepest ring that fits) that
+// minimises waves x tile width, i.e. the wave-quantisation loss of the
+// persistent grid; narrower tiles pay a small penalty for their lower operand
+// reuse (more bytes per MMA cycle).
+int choose_tc(const DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
+              TcConfig* out) {
+  double best = 1e300;
+  int best_bn = 0, best_stages = 0;
+  for (int bn : kTcTiles) {
+    if (o.tile_n && bn != o.tile_n) continue;
+    const int stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
+    if (stages == 0 || !tc_config_supported(bn, stages, realign) ||
+        tc_smem_bytes(bn, stages, realign) > d.smem_optin)
+      continue;
+    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + bn - 1) / bn);
+    const long long waves = (tiles + d.sm_count - 1) / d.sm_count;
+    const double reuse_penalty = 1.0 + 0.15 * (256 - bn) / 128.0;
+    const double cost = static_cast<double>(waves) * bn * reuse_penalty;
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_bn = bn;
+      best_stages = stages;
+    }
+  }
+  if (!best_bn) return FP8GEMM_EUNSUPPORTED;
+  const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + best_bn - 1) / best_bn);
+  out->bn = best_bn;
+  out->stages = best_stages;
+  out->realign = realign;
+  out->grid = static_cast<int>(std::min<long long>(tiles, d.sm_count));
+  out->group_m = 16;
+  return FP8GEMM_OK;
+}
+
 int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int K,
               const fp8gemm_options* opt, Plan* pl) {
-  fp8gemm_options o{};
+  fp8gemm_options o;
+  std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
   for (int r : o.reserved)
     if (r != 0) return FP8GEMM_EINVAL;
   std::memset(pl, 0, sizeof(*pl));
   if (M == 0 || N == 0) return FP8GEMM_OK;  // nothing to do
   const bool tma_ok = (K % 16 == 0) && (!x || aligned16(x)) && (!w || aligned16(w));
-  // K == 0 has nothing to load; the realigning variant then issues no copy
-  // and needs no tensor map.
-  const bool realign = o.force_realign != 0 || !tma_ok || K == 0;
-  const int num_kb = (K + 127) / 128;
   int path = o.path;
   if (path == FP8GEMM_PATH_AUTO) path = (M <= 64) ? FP8GEMM_PATH_DECODE : FP8GEMM_PATH_MAIN;
   if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
+  // Main path with rows TMA cannot tile: repitch into a workspace first,
+  // unless the caller forbids it or asks for the in-kernel loader.
+  const bool repitch = path == FP8GEMM_PATH_MAIN && K > 0 && !tma_ok && !o.force_realign &&
+                       !o.no_workspace && (o.workspace || d.pool);
+  // K == 0 has nothing to load; the realigning variant then issues no copy
+  // and needs no tensor map.
+  const bool realign = !repitch && (o.force_realign != 0 || !tma_ok || K == 0);
   pl->pub.path = path;
   pl->pub.realign = realign ? 1 : 0;
-  pl->pub.launches = 1;
+  pl->pub.repitch = repitch ? 1 : 0;
+  pl->pub.launches = repitch ? 2 : 1;
+  if (repitch) {
+    pl->Kp = (K + 15) & ~15;
+    pl->x_off = 0;
+    pl->w_off = align256(static_cast<size_t>(M) * pl->Kp);
+    pl->pub.workspace_bytes = pl->w_off + align256(static_cast<size_t>(N) * pl->Kp);
+  }
 
   if (path == FP8GEMM_PATH_MAIN) {
-    int bn = o.tile_n;
-    if (bn == 0) bn = (N <= 128) ? 128 : 256;
-    if (bn != 128 && bn != 256) return FP8GEMM_EUNSUPPORTED;
-    int stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
-    if (!tc_config_supported(bn, stages, realign) ||
-        tc_smem_bytes(bn, stages, realign) > d.smem_optin)
-      return FP8GEMM_EUNSUPPORTED;
-    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + bn - 1) / bn);
-    pl->tc.bn = bn;
-    pl->tc.stages = stages;
-    pl->tc.realign = realign;
-    pl->tc.grid = static_cast<int>(std::min<long long>(tiles, d.sm_count));
-    pl->tc.group_m = 16;
+    int st = choose_tc(d, M, N, realign, o, &pl->tc);
+    if (st != FP8GEMM_OK) return st;
+    int occ = 0;
+    if (tc_blocks_per_sm(pl->tc.bn, pl->tc.stages, realign, &occ) != cudaSuccess) {
+      cudaGetLastError();
+      occ = 0;
+    }
     pl->pub.tile_m = 128;
-    pl->pub.tile_n = bn;
-    pl->pub.stages = stages;
+    pl->pub.tile_n = pl->tc.bn;
+    pl->pub.stages = pl->tc.stages;
     pl->pub.splits = 1;
     pl->pub.grid = pl->tc.grid;
     pl->pub.cluster = 1;
     pl->pub.threads = tc_threads(realign);
-    pl->pub.smem_bytes = tc_smem_bytes(bn, stages, realign);
+    pl->pub.smem_bytes = tc_smem_bytes(pl->tc.bn, pl->tc.stages, realign);
+    pl->pub.occupancy = occ;
     return FP8GEMM_OK;
   }
 
-  // decode path
+  // decode path: pick (stages, splits) so that all CTAs are resident in as
+  // few waves as possible and each CTA streams as few K blocks as possible
   if (M > 128) return FP8GEMM_EUNSUPPORTED;
+  const int num_kb = (K + 127) / 128;
   const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
   const int n_tiles = (N + 127) / 128;
-  int best_s = 0, best_stages = 0;
+  int best_s = 0, best_stages = 0, best_occ = 0;
   double best_cost = 1e300;
-  const int stage_opts[] = {2, 3, 4, 6};
-  for (int stages : stage_opts) {
+  for (int stages : kDecStages) {
     if (o.stages && stages != o.stages) continue;
     if (!dec_config_supported(mp, stages, realign)) continue;
     const int occ = dec_occupancy(d, mp, stages, realign);
@@ -245,11 +296,13 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
       const long long waves = (ctas + slots - 1) / slots;
       const int per_cta = (num_kb + s - 1) / s;
       // a wave costs its longest CTA; shallow pipelines cost a little more
-      const double cost = static_cast<double>(waves) * (std::max(per_cta, 1) + 0.5 + 2.0 / stages);
+      const double cost =
+          static_cast<double>(waves) * (std::max(per_cta, 1) + 0.5 + 2.0 / stages);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best_s = s;
         best_stages = stages;
+        best_occ = occ;
       }
     }
   }
@@ -267,6 +320,7 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
   pl->pub.cluster = best_s;
   pl->pub.threads = dec_threads(realign);
   pl->pub.smem_bytes = dec_smem_bytes(mp, best_stages, realign);
+  pl->pub.occupancy = best_occ;
   return FP8GEMM_OK;
 }
 
@@ -284,6 +338,47 @@ int pointer_device(const void* p) {
   }
   if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return -1;
   return a.device;
+}
+
+// Enqueue the planned GEMM kernel.  xa / wa are the operands it reads (the
+// caller's, or their repitched copies) with row pitch Ka.
+int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* wa, int Ka,
+                const float* scale, void* y, int M, int N, cudaStream_t s) {
+  GemmArgs a{};
+  a.x = static_cast<const uint8_t*>(xa);
+  a.w = static_cast<const uint8_t*>(wa);
+  a.scale = scale;
+  a.y = static_cast<uint16_t*>(y);
+  a.M = M;
+  a.N = N;
+  a.K = Ka;
+  a.num_kb = (Ka + 127) / 128;
+  a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
+  a.err = d.err_word;
+  a.budget_ns = budget_ns();
+  // TMA descriptors are only meaningful on the TMA path (and need K >= 1);
+  // the realigning producer reads x and w through plain pointers.
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  const bool use_tma = !pl.pub.realign && Ka > 0;
+  cudaError_t e;
+  if (pl.pub.path == FP8GEMM_PATH_MAIN) {
+    if (use_tma && (encode_operand(&tmA, xa, M, Ka, 128) != FP8GEMM_OK ||
+                    encode_operand(&tmB, wa, N, Ka, pl.tc.bn) != FP8GEMM_OK))
+      return FP8GEMM_ELAUNCH;
+    e = launch_tc(tmA, tmB, a, pl.tc, s);
+  } else {
+    if (use_tma && (encode_operand(&tmA, wa, N, Ka, 128) != FP8GEMM_OK ||
+                    encode_operand(&tmB, xa, M, Ka, pl.dec.mp) != FP8GEMM_OK))
+      return FP8GEMM_ELAUNCH;
+    e = launch_decode(tmA, tmB, a, pl.dec, s);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  return FP8GEMM_OK;
 }
 
 }  // namespace
@@ -306,8 +401,8 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb))
     return FP8GEMM_EINVAL;
   const int dev = pointer_device(y);
-  if (dev < 0 || pointer_device(scale) != dev || (K > 0 && (pointer_device(x) != dev ||
-                                                           pointer_device(w) != dev)))
+  if (dev < 0 || pointer_device(scale) != dev ||
+      (K > 0 && (pointer_device(x) != dev || pointer_device(w) != dev)))
     return FP8GEMM_EINVAL;
   DevState* d = nullptr;
   int st = device_state(dev, &d);
@@ -319,47 +414,57 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   Plan pl;
   st = make_plan(*d, x, w, M, N, K, opt, &pl);
   if (st != FP8GEMM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!pl.pub.repitch) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
 
-  GemmArgs a{};
-  a.x = static_cast<const uint8_t*>(x);
-  a.w = static_cast<const uint8_t*>(w);
-  a.scale = scale;
-  a.y = static_cast<uint16_t*>(y);
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.num_kb = (K + 127) / 128;
-  a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
-  a.err = d->err_word;
-  a.budget_ns = budget_ns();
-
-  // TMA descriptors are only meaningful on the TMA path (and need K >= 1);
-  // the realigning producer reads x and w through plain pointers.
-  CUtensorMap tmA, tmB;
-  std::memset(&tmA, 0, sizeof(tmA));
-  std::memset(&tmB, 0, sizeof(tmB));
-  const bool use_tma = !pl.pub.realign && K > 0;
-  cudaError_t e;
-  if (pl.pub.path == FP8GEMM_PATH_MAIN) {
-    if (use_tma) {
-      if (encode_operand(&tmA, x, M, K, 128) != FP8GEMM_OK ||
-          encode_operand(&tmB, w, N, K, pl.tc.bn) != FP8GEMM_OK)
-        return FP8GEMM_ELAUNCH;
-    }
-    e = launch_tc(tmA, tmB, a, pl.tc, reinterpret_cast<cudaStream_t>(stream));
+  // repitch x and w into the workspace, then run the TMA kernel on the copies
+  const size_t need = pl.pub.workspace_bytes;
+  uint8_t* ws = nullptr;
+  bool pooled = false;
+  if (opt && opt->workspace) {
+    ws = static_cast<uint8_t*>(opt->workspace);
+    if (opt->workspace_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+        pointer_device(ws) != dev || overlaps(ws, need, y, yb) || overlaps(ws, need, x, xb) ||
+        overlaps(ws, need, w, wb) || overlaps(ws, need, scale, sb))
+      return FP8GEMM_EINVAL;
   } else {
-    if (use_tma) {
-      if (encode_operand(&tmA, w, N, K, 128) != FP8GEMM_OK ||
-          encode_operand(&tmB, x, M, K, pl.dec.mp) != FP8GEMM_OK)
-        return FP8GEMM_ELAUNCH;
+    void* p = nullptr;
+    if (cudaMallocFromPoolAsync(&p, need, d->pool, s) != cudaSuccess) {
+      // no memory for a workspace: load the unaligned rows in the kernel instead
+      cudaGetLastError();
+      fp8gemm_options o2;
+      std::memset(&o2, 0, sizeof(o2));
+      if (opt) o2 = *opt;
+      o2.no_workspace = 1;
+      o2.workspace = nullptr;
+      o2.workspace_bytes = 0;
+      st = make_plan(*d, x, w, M, N, K, &o2, &pl);
+      if (st != FP8GEMM_OK) return st;
+      return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
     }
-    e = launch_decode(tmA, tmB, a, pl.dec, reinterpret_cast<cudaStream_t>(stream));
+    ws = static_cast<uint8_t*>(p);
+    pooled = true;
   }
-  if (e != cudaSuccess) {
+  RepitchArgs r{};
+  r.x = static_cast<const uint8_t*>(x);
+  r.w = static_cast<const uint8_t*>(w);
+  r.xo = ws + pl.x_off;
+  r.wo = ws + pl.w_off;
+  r.K = K;
+  r.Kp = pl.Kp;
+  r.chunks_x = static_cast<long long>(M) * (pl.Kp / 16);
+  r.chunks_w = static_cast<long long>(N) * (pl.Kp / 16);
+  if (launch_repitch(r, d->sm_count, s) != cudaSuccess) {
     cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
+    st = FP8GEMM_ELAUNCH;
+  } else {
+    st = launch_gemm(pl, *d, r.xo, r.wo, pl.Kp, scale, y, M, N, s);
   }
-  return FP8GEMM_OK;
+  if (pooled && cudaFreeAsync(ws, s) != cudaSuccess) {
+    cudaGetLastError();
+    if (st == FP8GEMM_OK) st = FP8GEMM_ELAUNCH;
+  }
+  return st;
 }
 
 extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,
@@ -378,6 +483,13 @@ extern "C" int fp8_gemm_plan(int device, const void* x, const void* w, int M, in
   if (st != FP8GEMM_OK) return st;
   *out = pl.pub;
   return FP8GEMM_OK;
+}
+
+extern "C" size_t fp8_gemm_workspace_bytes(int device, const void* x, const void* w, int M, int N,
+                                           int K, const fp8gemm_options* opt) {
+  fp8gemm_plan p;
+  if (fp8_gemm_plan(device, x, w, M, N, K, opt, &p) != FP8GEMM_OK) return 0;
+  return p.workspace_bytes;
 }
 
 extern "C" int fp8_gemm_check_device_error(fp8gemm_stream_t stream) {
@@ -436,7 +548,7 @@ extern "C" int fp8_gemm_selftest_wait_timeout(unsigned long long budget, fp8gemm
 extern "C" const char* fp8_gemm_status_string(int status) {
   switch (status) {
     case FP8GEMM_OK: return "ok";
-    case FP8GEMM_EINVAL: return "invalid argument (null or host pointer, bad size, y aliases an input)";
+    case FP8GEMM_EINVAL: return "invalid argument (null or host pointer, bad size, overlapping buffers)";
     case FP8GEMM_EALIGN: return "misaligned pointer (scale needs 4 bytes, y needs 2 bytes)";
     case FP8GEMM_EDEVICE: return "no usable device (needs compute capability 10.3)";
     case FP8GEMM_ELAUNCH: return "CUDA launch or runtime call failed";

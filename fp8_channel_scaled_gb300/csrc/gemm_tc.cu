@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
             break;
           }
           load_tile_realign<kBM, 128, 4>(sA(stage), p.x, p.M, p.K, mb * kBM, kb * kBK, ptid);
-          load_tile_realign<BN, 128, 4>(sB(stage), p.w, p.N, p.K, nb * BN, kb * kBK, ptid);
+          load_tile_realign<BN, 128, ((BN * 8 / 128) % 4 == 0) ? 4 : 2>(sB(stage), p.w, p.N, p.K,
+                                                                       nb * BN, kb * kBK, ptid);
           fence_proxy_async_smem();
           mbar_arrive(full_bar(stage));
           if (++stage == STAGES) {
@@ -314,10 +315,14 @@ Entry make_entry() {
                Cfg<BN, S, R>::kSmemBytes, Cfg<BN, S, R>::kThreads};
 }
 
+// N tiles and pipeline depths that are built: for each N tile the deepest
+// ring that fits in shared memory (and one shallower ring), plus the
+// realigning-producer variants used when no workspace can be had.
 const Entry kEntries[] = {
-    make_entry<256, 4, false>(), make_entry<256, 3, false>(), make_entry<128, 6, false>(),
-    make_entry<128, 4, false>(), make_entry<256, 4, true>(),  make_entry<256, 3, true>(),
-    make_entry<128, 6, true>(),  make_entry<128, 4, true>(),
+    make_entry<256, 4, false>(), make_entry<256, 3, false>(), make_entry<224, 5, false>(),
+    make_entry<224, 4, false>(), make_entry<192, 5, false>(), make_entry<160, 6, false>(),
+    make_entry<128, 7, false>(), make_entry<128, 6, false>(), make_entry<256, 4, true>(),
+    make_entry<224, 4, true>(),  make_entry<128, 6, true>(),
 };
 
 const Entry* find(int bn, int stages, bool realign) {
@@ -345,6 +350,13 @@ int tc_max_stages(int bn, bool realign, int smem_optin) {
     if (e.bn == bn && e.realign == realign && e.smem <= smem_optin && e.stages > best)
       best = e.stages;
   return best;
+}
+
+cudaError_t tc_blocks_per_sm(int bn, int stages, bool realign, int* out) {
+  const Entry* e = find(bn, stages, realign);
+  if (!e) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, e->fn, e->threads,
+                                                       static_cast<size_t>(e->smem));
 }
 
 cudaError_t tc_prepare(int bn, int stages, bool realign) {

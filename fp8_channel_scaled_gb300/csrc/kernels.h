@@ -35,6 +35,7 @@ int tc_smem_bytes(int bn, int stages, bool realign);
 int tc_threads(bool realign);
 int tc_max_stages(int bn, bool realign, int smem_optin);
 cudaError_t tc_prepare(int bn, int stages, bool realign);  // per device, before first launch
+cudaError_t tc_blocks_per_sm(int bn, int stages, bool realign, int* out);
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                       const TcConfig& c, cudaStream_t s);
 
@@ -57,5 +58,17 @@ cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits
 cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                           const DecConfig& c, cudaStream_t s);
 
+
+// ---- repitch of unaligned operands into a workspace ------------------------
+struct RepitchArgs {
+  const uint8_t* x;      // [M, K], any alignment
+  const uint8_t* w;      // [N, K], any alignment
+  uint8_t* xo;           // [M, Kp], 16-byte aligned
+  uint8_t* wo;           // [N, Kp], 16-byte aligned
+  int K, Kp;             // Kp = round_up(K, 16)
+  long long chunks_x;    // M * Kp / 16
+  long long chunks_w;    // N * Kp / 16
+};
+cudaError_t launch_repitch(const RepitchArgs& a, int sm_count, cudaStream_t s);
 
 }  // namespace fp8g

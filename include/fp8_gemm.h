@@ -19,9 +19,14 @@
  *   - Streams: `stream` is a CUDA runtime stream handle (cudaStream_t); NULL
  *     means the legacy default stream.  Compute calls are asynchronous with
  *     respect to the host and never synchronise.
- *   - Ownership: the caller owns every buffer.  The library allocates no
- *     device memory per call; it keeps, per device, only its properties and
- *     a 4-byte device error word (see fp8_gemm_check_device_error).
+ *   - Ownership: the caller owns every buffer.  The library keeps, per
+ *     device, its properties, a 4-byte device error word (see
+ *     fp8_gemm_check_device_error) and a private stream-ordered memory pool.
+ *     The only device memory a call may take is the repitch workspace of the
+ *     main path (see fp8_gemm_workspace_bytes): from the caller when
+ *     fp8gemm_options.workspace is given, else from that pool with
+ *     cudaMallocFromPoolAsync / cudaFreeAsync on the call's stream, so calls
+ *     on different streams never share it.
  *   - Nothing derived from the data is ever cached: each call reads x, w
  *     and weight_scale as they are when the kernel runs (the pages' stale
  *     padded-input failure, "qwen3.8-max" page, odd-K pad-cache paragraph,
@@ -30,6 +35,8 @@
  */
 #ifndef FP8_GEMM_H
 #define FP8_GEMM_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -64,12 +71,16 @@ enum {
  */
 typedef struct {
     int path;           /* FP8GEMM_PATH_* */
-    int force_realign;  /* 1: load operands with the realigning producer even
-                           when TMA could (tests the K % 16 != 0 loader) */
-    int tile_n;         /* main path N tile: 0 auto, 128 or 256 */
+    int force_realign;  /* 1: load operands with the in-kernel realigning
+                           producer even when TMA could (tests that loader) */
+    int tile_n;         /* main path N tile: 0 auto, or 128, 160, 192, 224, 256 */
     int stages;         /* pipeline depth: 0 auto */
     int splits;         /* decode path K splits (cluster size): 0 auto, 1..8 */
-    int reserved[3];    /* must be zero */
+    int no_workspace;   /* 1: never repitch; rows TMA cannot tile are then
+                           loaded by the in-kernel realigning producer */
+    int reserved[2];    /* must be zero */
+    void *workspace;    /* optional caller workspace (device, 256-byte aligned) */
+    size_t workspace_bytes; /* its size; must be >= fp8_gemm_workspace_bytes() */
 } fp8gemm_options;
 
 /* What a call with the same arguments would launch (see fp8_gemm_plan). */
@@ -84,7 +95,10 @@ typedef struct {
     int cluster;        /* CTAs per cluster */
     int threads;        /* threads per CTA */
     int smem_bytes;     /* dynamic shared memory per CTA */
-    int launches;       /* kernels launched by one call (0 or 1) */
+    int launches;       /* kernels launched by one call (0, 1, or 2 with repitch) */
+    int repitch;        /* 1: operands are first copied to a 16-byte pitch */
+    int occupancy;      /* resident CTAs per SM of the GEMM kernel */
+    size_t workspace_bytes; /* device workspace the call needs (0 = none) */
 } fp8gemm_plan;
 
 /*
@@ -98,10 +112,13 @@ typedef struct {
  *   M,N,K  >= 0.  M == 0 or N == 0: nothing is launched.  K == 0: y = 0.
  *
  * Rows whose pitch K is not a multiple of 16 bytes (e.g. K = 4127), or
- * operands not 16-byte aligned, are loaded by an in-kernel realigning
- * producer; bytes past K are treated as zeros, which adds exactly nothing
- * (the zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
- * paragraph).  No padded copy is made.
+ * operands not 16-byte aligned, cannot be tiled by TMA.  On the main path
+ * they are first copied by a repitch kernel into a workspace with a
+ * 16-byte pitch and zero pad bytes (two launches); on the decode path, or
+ * with no_workspace, an in-kernel realigning producer loads them directly.
+ * Either way bytes past K count as zeros, which adds exactly nothing (the
+ * zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
+ * paragraph).  Nothing is cached between calls.
  *
  * Returns FP8GEMM_OK once the kernel is enqueued.  Errors inside the kernel
  * (a bounded wait that ran out) are reported by fp8_gemm_check_device_error.
@@ -122,6 +139,15 @@ int fp8_gemm_scaled_ex(const void *x, const void *w, const float *scale, void *y
  */
 int fp8_gemm_plan(int device, const void *x, const void *w, int M, int N, int K,
                   const fp8gemm_options *opt, fp8gemm_plan *out);
+
+/*
+ * fp8_gemm_workspace_bytes -- device workspace (bytes) a call with these
+ * arguments needs for its repitch pass; 0 when it needs none.  x and w are
+ * used only for their alignment and may be NULL (taken as 16-byte aligned).
+ * Returns 0 also for invalid arguments.
+ */
+size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M, int N,
+                                int K, const fp8gemm_options *opt);
 
 /*
  * fp8_gemm_check_device_error -- synchronise `stream`, read and clear the

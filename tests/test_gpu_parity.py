@@ -76,12 +76,48 @@ def test_main_path_shapes(M, N, K):
     check_full(x, w, s, Options(path=PATH_MAIN), what=f"main {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("bn", [128, 256])
-@pytest.mark.parametrize("realign", [False, True])
-def test_main_path_tiles_and_loaders(bn, realign):
+@pytest.mark.parametrize("bn", [128, 160, 192, 224, 256])
+def test_main_path_tiles(bn):
     x, w, s = synth.make_inputs(300, 520, 640, seed=5)
-    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn, force_realign=realign),
-               what=f"main bn={bn} realign={realign}")
+    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn), what=f"main bn={bn}")
+
+
+@pytest.mark.parametrize("bn", [128, 224, 256])
+def test_main_path_realigning_loader(bn):
+    x, w, s = synth.make_inputs(300, 520, 640, seed=5)
+    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn, force_realign=True),
+               what=f"main realign bn={bn}")
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 264, 4127), (256, 300, 17), (129, 1000, 1000)])
+def test_repitch_equals_in_kernel_loader_bitwise(M, N, K):
+    x, w, s = synth.make_inputs(M, N, K, seed=K)
+    p = fg.plan(M, N, K, Options(path=PATH_MAIN))
+    assert p.repitch == 1 and p.launches == 2
+    assert p.workspace_bytes >= M * ((K + 15) // 16 * 16) + N * ((K + 15) // 16 * 16)
+    a = run(x, w, s, Options(path=PATH_MAIN))
+    b = run(x, w, s, Options(path=PATH_MAIN, no_workspace=True))
+    assert np.array_equal(a, b)
+    compare(a, oracle.linear(x, w, s), f"repitch {M}x{N}x{K}")
+
+
+def test_caller_workspace():
+    M, N, K = 200, 264, 4127
+    x, w, s = synth.make_inputs(M, N, K, seed=2)
+    need = fg.fp8_gemm_workspace_bytes(torch.cuda.current_device(), M, N, K)
+    assert need > 0
+    ws = torch.full((need + 512,), 0xAB, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 255) // 256 * 256
+    got = run(x, w, s, Options(workspace=base, workspace_bytes=need))
+    compare(got, oracle.linear(x, w, s), "caller workspace")
+    # a workspace that is too small is refused before anything runs
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(workspace=base, workspace_bytes=need - 256))
+    assert e.value.status == 1
+    # aligned operands need no workspace
+    assert fg.fp8_gemm_workspace_bytes(torch.cuda.current_device(), M, N, 4096) == 0
 
 
 # ------------------------------------------------------------------ decode path shapes and tails
@@ -182,10 +218,18 @@ def test_unaligned_operand_bases_and_poisoned_neighbours(path, offset):
     wd.copy_(to_dev(w))
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     p = fg.plan(M, N, K, Options(path=path), x=xd, w=wd)
-    assert p.realign == 1
+    if path == PATH_MAIN:
+        assert p.repitch == 1 and p.realign == 0 and p.launches == 2
+    else:
+        assert p.realign == 1 and p.repitch == 0
     fg.fp8_gemm_scaled_ex(xd, wd, to_dev(s), y, Options(path=path))
     fg.check_device_error()
     compare(y_bits(y), oracle.linear(x, w, s), f"offset {offset}")
+    if path == PATH_MAIN:  # the in-kernel loader gives the same bits
+        y2 = torch.empty_like(y)
+        fg.fp8_gemm_scaled_ex(xd, wd, to_dev(s), y2, Options(path=path, no_workspace=True))
+        fg.check_device_error()
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
 def test_output_guard_bands_untouched():

@@ -33,9 +33,10 @@ def test_workload(key):
     xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
     y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
     p = fg.plan(wl.M, wl.N, wl.K, x=xd, w=wd)
-    assert p.launches == 1
     assert p.path == (fg.PATH_DECODE if wl.M <= 64 else fg.PATH_MAIN)
-    assert p.realign == (1 if wl.K % 16 else 0)
+    odd = wl.K % 16 != 0
+    assert p.repitch == int(odd) and p.realign == 0
+    assert p.launches == (2 if odd else 1)
     fg.fp8_gemm_scaled(xd, wd, sd, y)
     fg.check_device_error()
     got = y_bits(y)
