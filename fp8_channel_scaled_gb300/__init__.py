@@ -12,6 +12,7 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     FP8GemmError,
+    NOALLOC_WORKSPACE_BYTES,
     Options,
     Plan,
     PATH_AUTO,
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     fp8_gemm_plan,
     fp8_gemm_scaled,
     fp8_gemm_scaled_ex,
+    fp8_gemm_scaled_noalloc,
     fp8_gemm_selftest_wait_timeout,
     fp8_gemm_set_wait_budget_ns,
     fp8_gemm_status_string,

@@ -11,7 +11,8 @@ _LIB_PATH = _PKG / "_lib" / "libfp8gemm.so"
 
 PATH_AUTO, PATH_MAIN, PATH_DECODE = 0, 1, 2
 STATUS = {0: "OK", 1: "EINVAL", 2: "EALIGN", 3: "EDEVICE", 4: "ELAUNCH", 5: "ETIMEOUT",
-          6: "EUNSUPPORTED"}
+          6: "EUNSUPPORTED", 7: "ESIZE"}
+NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
 class FP8GemmError(RuntimeError):
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
         vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
         L.fp8_gemm_scaled.argtypes = [vp, vp, vp, vp, i, i, i, st]
         L.fp8_gemm_scaled_ex.argtypes = [vp, vp, vp, vp, i, i, i, ctypes.POINTER(_COptions), st]
+        L.fp8_gemm_scaled_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, st]
         L.fp8_gemm_plan.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions),
                                     ctypes.POINTER(_CPlan)]
         L.fp8_gemm_workspace_bytes.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions)]
@@ -108,7 +110,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_status_string.restype = ctypes.c_char_p
         L.fp8_gemm_last_device_error_bits.argtypes = []
         L.fp8_gemm_last_device_error_bits.restype = ctypes.c_uint
-        for f in ("fp8_gemm_scaled", "fp8_gemm_scaled_ex", "fp8_gemm_plan",
+        for f in ("fp8_gemm_scaled", "fp8_gemm_scaled_ex", "fp8_gemm_scaled_noalloc",
+                  "fp8_gemm_plan",
                   "fp8_gemm_check_device_error", "fp8_gemm_set_wait_budget_ns",
                   "fp8_gemm_selftest_wait_timeout", "fp8_gemm_version"):
             getattr(L, f).restype = ctypes.c_int
@@ -170,6 +173,15 @@ def fp8_gemm_scaled_ex(x, w, scale, y, options: Options | None = None, stream=No
     o = (options or Options())._c()
     _check(lib().fp8_gemm_scaled_ex(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
                                     ctypes.byref(o), _stream_handle(stream)), "fp8_gemm_scaled_ex")
+
+
+def fp8_gemm_scaled_noalloc(x, w, scale, y, stream=None) -> None:
+    """As fp8_gemm_scaled, but allocates no device memory: any repitch copies go
+    into the library's static 32 MiB device workspace (see include/fp8_gemm.h).
+    Calls that overlap on the GPU race on that workspace."""
+    M, N, K = _shapes(x, w, scale, y)
+    _check(lib().fp8_gemm_scaled_noalloc(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
+                                         _stream_handle(stream)), "fp8_gemm_scaled_noalloc")
 
 
 def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None = None,

@@ -51,7 +51,9 @@ struct DevState {
   int sm_count = 0;
   int smem_optin = 0;
   unsigned* err_word = nullptr;
-  cudaMemPool_t pool = nullptr;  // private stream-ordered pool for repitch workspaces
+  cudaMemPool_t pool = nullptr;  // private stream-ordered pool for repitch workspaces,
+  bool pool_failed = false;      // created on first pooled use, never by the no-alloc entry
+  void* noalloc_ws = nullptr;    // device address of g_noalloc_workspace on this device
 };
 
 std::mutex g_mu;
@@ -82,8 +84,8 @@ const int kTcStages[] = {3, 4, 5, 6, 7};
 const int kDecMp[] = {32, 64, 128};
 const int kDecStages[] = {2, 3, 4, 6};
 
-// Per-device set-up, once: properties, error word address, kernel attributes,
-// workspace pool.
+// Per-device set-up, once: properties, error word address, kernel attributes.
+// It allocates nothing; the workspace pool is created on first pooled use.
 int device_state(int dev, DevState** out) {
   if (dev < 0 || dev >= kMaxDevices) return FP8GEMM_EDEVICE;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -134,6 +136,15 @@ int device_state(int dev, DevState** out) {
           return d.status;
         }
   }
+  d.status = FP8GEMM_OK;
+  return d.status;
+}
+
+// The device's private workspace pool, created on first use; nullptr if it
+// cannot be created (calls then load unaligned rows in the kernel instead).
+cudaMemPool_t workspace_pool(DevState& d, int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (d.pool || d.pool_failed) return d.pool;
   cudaMemPoolProps props;
   std::memset(&props, 0, sizeof(props));
   props.allocType = cudaMemAllocationTypePinned;
@@ -144,10 +155,10 @@ int device_state(int dev, DevState** out) {
     cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
   } else {
     cudaGetLastError();
-    d.pool = nullptr;  // calls then fall back to the realigning producer
+    d.pool = nullptr;
+    d.pool_failed = true;
   }
-  d.status = FP8GEMM_OK;
-  return d.status;
+  return d.pool;
 }
 
 // TMA descriptor of a row-major byte matrix [rows, K], box [box_rows, 128],
@@ -240,7 +251,7 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
   // Main path with rows TMA cannot tile: repitch into a workspace first,
   // unless the caller forbids it or asks for the in-kernel loader.
   const bool repitch = path == FP8GEMM_PATH_MAIN && K > 0 && !tma_ok && !o.force_realign &&
-                       !o.no_workspace && (o.workspace || d.pool);
+                       !o.no_workspace && (o.workspace || !d.pool_failed);
   // K == 0 has nothing to load; the realigning variant then issues no copy
   // and needs no tensor map.
   const bool realign = !repitch && (o.force_realign != 0 || !tma_ok || K == 0);
@@ -382,6 +393,32 @@ int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* w
 }
 
 }  // namespace
+
+// Repitch workspace of fp8_gemm_scaled_noalloc, for callers that cannot
+// allocate device memory.  In host code this name is only a stand-in: its
+// device address comes from cudaGetSymbolAddress (noalloc_workspace below).
+static __device__ __align__(256) unsigned char g_noalloc_workspace[FP8GEMM_NOALLOC_WORKSPACE_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_workspace on device `dev`, which must be the
+// current device; looked up on the first call on that device.
+int noalloc_workspace(DevState& d, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!d.noalloc_ws) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return FP8GEMM_ELAUNCH;
+    }
+    d.noalloc_ws = p;
+  }
+  *out = static_cast<uint8_t*>(d.noalloc_ws);
+  return FP8GEMM_OK;
+}
+
+}  // namespace
 }  // namespace fp8g
 
 using namespace fp8g;
@@ -429,7 +466,8 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
       return FP8GEMM_EINVAL;
   } else {
     void* p = nullptr;
-    if (cudaMallocFromPoolAsync(&p, need, d->pool, s) != cudaSuccess) {
+    cudaMemPool_t pool = workspace_pool(*d, dev);
+    if (!pool || cudaMallocFromPoolAsync(&p, need, pool, s) != cudaSuccess) {
       // no memory for a workspace: load the unaligned rows in the kernel instead
       cudaGetLastError();
       fp8gemm_options o2;
@@ -465,6 +503,63 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
     if (st == FP8GEMM_OK) st = FP8GEMM_ELAUNCH;
   }
   return st;
+}
+
+// Same layer as fp8_gemm_scaled for callers that must not allocate: the
+// repitch copies (if any) go into the static g_noalloc_workspace instead of a
+// pool or caller buffer.  Calls that overlap on the GPU race on that array.
+extern "C" int fp8_gemm_scaled_noalloc(const void* x, const void* w, const float* scale, void* y,
+                                       int M, int N, int K, fp8gemm_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8GEMM_EINVAL;
+  if (M == 0 || N == 0) return FP8GEMM_OK;
+  if (!scale || !y || (K > 0 && (!x || !w))) return FP8GEMM_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+    return FP8GEMM_EALIGN;
+  const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K);
+  const size_t wb = static_cast<size_t>(N) * static_cast<size_t>(K);
+  const size_t yb = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
+  const size_t sb = static_cast<size_t>(N) * 4u;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb))
+    return FP8GEMM_EINVAL;
+  const int dev = pointer_device(y);
+  if (dev < 0 || pointer_device(scale) != dev ||
+      (K > 0 && (pointer_device(x) != dev || pointer_device(w) != dev)))
+    return FP8GEMM_EINVAL;
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  uint8_t* ws = nullptr;
+  st = noalloc_workspace(*d, &ws);
+  if (st != FP8GEMM_OK) return st;
+  // plan as fp8_gemm_scaled would, with the static array as the workspace
+  fp8gemm_options o;
+  std::memset(&o, 0, sizeof(o));
+  o.workspace = ws;
+  o.workspace_bytes = FP8GEMM_NOALLOC_WORKSPACE_BYTES;
+  Plan pl;
+  st = make_plan(*d, x, w, M, N, K, &o, &pl);
+  if (st != FP8GEMM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!pl.pub.repitch) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
+  if (pl.pub.workspace_bytes > FP8GEMM_NOALLOC_WORKSPACE_BYTES) return FP8GEMM_ESIZE;
+  RepitchArgs r{};
+  r.x = static_cast<const uint8_t*>(x);
+  r.w = static_cast<const uint8_t*>(w);
+  r.xo = ws + pl.x_off;
+  r.wo = ws + pl.w_off;
+  r.K = K;
+  r.Kp = pl.Kp;
+  r.chunks_x = static_cast<long long>(M) * (pl.Kp / 16);
+  r.chunks_w = static_cast<long long>(N) * (pl.Kp / 16);
+  if (launch_repitch(r, d->sm_count, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  return launch_gemm(pl, *d, r.xo, r.wo, pl.Kp, scale, y, M, N, s);
 }
 
 extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,
@@ -554,6 +649,9 @@ extern "C" const char* fp8_gemm_status_string(int status) {
     case FP8GEMM_ELAUNCH: return "CUDA launch or runtime call failed";
     case FP8GEMM_ETIMEOUT: return "a kernel gave up a bounded wait; its output is invalid";
     case FP8GEMM_EUNSUPPORTED: return "requested configuration is not built";
+    case FP8GEMM_ESIZE:
+      return "fp8_gemm_scaled_noalloc: the repitch workspace this call needs exceeds "
+             "FP8GEMM_NOALLOC_WORKSPACE_BYTES";
     default: return "unknown status";
   }
 }

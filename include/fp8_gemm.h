@@ -55,7 +55,9 @@ typedef enum {
     FP8GEMM_EDEVICE = 3,   /* no CUDA device, or not compute capability 10.3 */
     FP8GEMM_ELAUNCH = 4,   /* the CUDA launch (or a CUDA runtime call) failed */
     FP8GEMM_ETIMEOUT = 5,  /* a kernel gave up a bounded wait (results invalid) */
-    FP8GEMM_EUNSUPPORTED = 6 /* the options ask for a configuration not built */
+    FP8GEMM_EUNSUPPORTED = 6, /* the options ask for a configuration not built */
+    FP8GEMM_ESIZE = 7      /* fp8_gemm_scaled_noalloc: workspace needed exceeds
+                              FP8GEMM_NOALLOC_WORKSPACE_BYTES */
 } fp8gemm_status;
 
 /* Kernel path. */
@@ -148,6 +150,39 @@ int fp8_gemm_plan(int device, const void *x, const void *w, int M, int N, int K,
  */
 size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M, int N,
                                 int K, const fp8gemm_options *opt);
+
+/*
+ * fp8_gemm_scaled_noalloc -- the same layer as fp8_gemm_scaled, for callers
+ * that must not allocate device memory: code that runs where cudaMalloc is
+ * forbidden or unsafe (inside another allocator's or framework's memory
+ * accounting, in a context whose memory is fixed up front, on a path that
+ * may not synchronise the device).  It calls no cudaMalloc, cudaFree, pool
+ * or other allocating routine.  The pages have no counterpart; it is an
+ * addition of this library.
+ *
+ * When the main path has to repitch x and w (rows not 16-byte aligned, e.g.
+ * K = 4127), the copies go into one static device array of
+ * FP8GEMM_NOALLOC_WORKSPACE_BYTES (32 MiB) that every GPU which loads the
+ * library holds until the process exits.  The repitch kernel writes every
+ * byte of it that the GEMM then reads, pad bytes included, so nothing has to
+ * start at zero.  Calls that need more than that (M * Kp + N * Kp bytes,
+ * Kp = round_up(K, 16), each part rounded up to 256 bytes) return
+ * FP8GEMM_ESIZE and launch nothing.  Calls that need no repitch launch
+ * exactly what fp8_gemm_scaled launches.
+ *
+ * All calls on a device share the one array and it keeps the last call's
+ * contents: two calls that overlap on the GPU (different streams with no
+ * ordering between them) race on it and may produce wrong results.  Order
+ * them on one stream, or with events.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current), which may load the
+ * library's module; make that first call before any stream capture.
+ * Arguments, layouts and error behaviour are those of fp8_gemm_scaled.
+ */
+#define FP8GEMM_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+int fp8_gemm_scaled_noalloc(const void *x, const void *w, const float *scale, void *y,
+                            int M, int N, int K, fp8gemm_stream_t stream);
 
 /*
  * fp8_gemm_check_device_error -- synchronise `stream`, read and clear the
