@@ -25,7 +25,8 @@ class FP8GemmError(RuntimeError):
 class _COptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("force_realign", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("splits", ctypes.c_int),
-                ("no_workspace", ctypes.c_int), ("reserved", ctypes.c_int * 2),
+                ("no_workspace", ctypes.c_int), ("mma_ctas", ctypes.c_int),
+                ("reserved", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
@@ -46,6 +47,7 @@ class Options:
     stages: int = 0
     splits: int = 0
     no_workspace: bool = False
+    mma_ctas: int = 0           # main path: 0 auto, 1 one-CTA tiles, 2 CTA-pair tiles
     workspace: int = 0          # device pointer (e.g. tensor.data_ptr()), 0 = library pool
     workspace_bytes: int = 0
 
@@ -54,6 +56,7 @@ class Options:
         o.path, o.force_realign = int(self.path), int(bool(self.force_realign))
         o.tile_n, o.stages, o.splits = int(self.tile_n), int(self.stages), int(self.splits)
         o.no_workspace = int(bool(self.no_workspace))
+        o.mma_ctas = int(self.mma_ctas)
         o.workspace = int(self.workspace) or None
         o.workspace_bytes = int(self.workspace_bytes)
         return o

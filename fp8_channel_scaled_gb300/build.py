@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 OBJ_DIR = ROOT / "_build" / "fp8gemm"
 LIB_DIR = PKG / "_lib"
 LIB = LIB_DIR / "libfp8gemm.so"
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_decode.cu", "repitch.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_tc2.cu", "gemm_decode.cu", "repitch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                  "-I", str(INCLUDE), "-I", str(CSRC)]

@@ -81,8 +81,9 @@ unsigned long long budget_ns() {
 
 const int kTcTiles[] = {256, 224, 192, 160, 128};
 const int kTcStages[] = {3, 4, 5, 6, 7};
+const int kTc2Stages[] = {6, 7, 8};
 const int kDecMp[] = {32, 64, 128};
-const int kDecStages[] = {2, 3, 4, 6};
+const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
 // Per-device set-up, once: properties, error word address, kernel attributes.
 // It allocates nothing; the workspace pool is created on first pooled use.
@@ -122,6 +123,12 @@ int device_state(int dev, DevState** out) {
     }
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
+  for (int bn : kTcTiles)
+    for (int s : kTc2Stages)
+      if (tc2_config_supported(bn, s) && tc2_prepare(bn, s) != cudaSuccess) {
+        cudaGetLastError();
+        return d.status;
+      }
   for (bool r : {false, true}) {
     for (int bn : kTcTiles)
       for (int s : kTcStages)
@@ -201,37 +208,62 @@ int dec_occupancy(const DevState& d, int mp, int stages, bool realign) {
   return blocks;
 }
 
-// Main path tile choice: the N tile (with the deepest ring that fits) that
-// minimises waves x tile width, i.e. the wave-quantisation loss of the
-// persistent grid; narrower tiles pay a small penalty for their lower operand
-// reuse (more bytes per MMA cycle).
+// Main path tile choice.  For each N tile (with the deepest ring that fits)
+// and each tile kind -- one-CTA 128-row tiles or CTA-pair 256-row tiles --
+// estimate waves x tile width, i.e. the wave quantisation of the persistent
+// grid (a pair's 256 x BN tile takes about as long as one CTA's 128 x BN
+// tile).  One-CTA tiles pay for the larger share of B each SM stages and
+// reads (measured about 1.3x slower per tile); narrower tiles pay for their
+// lower operand reuse.  The realigning producer exists for one-CTA tiles only.
 int choose_tc(const DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
               TcConfig* out) {
   double best = 1e300;
-  int best_bn = 0, best_stages = 0;
-  for (int bn : kTcTiles) {
-    if (o.tile_n && bn != o.tile_n) continue;
-    const int stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
-    if (stages == 0 || !tc_config_supported(bn, stages, realign) ||
-        tc_smem_bytes(bn, stages, realign) > d.smem_optin)
-      continue;
-    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + bn - 1) / bn);
-    const long long waves = (tiles + d.sm_count - 1) / d.sm_count;
-    const double reuse_penalty = 1.0 + 0.15 * (256 - bn) / 128.0;
-    const double cost = static_cast<double>(waves) * bn * reuse_penalty;
-    if (cost < best - 1e-9) {
-      best = cost;
-      best_bn = bn;
-      best_stages = stages;
+  TcConfig pick{};
+  for (int ctas : {2, 1}) {
+    if (o.mma_ctas && ctas != o.mma_ctas) continue;
+    if (ctas == 2 && realign) continue;
+    for (int bn : kTcTiles) {
+      if (o.tile_n && bn != o.tile_n) continue;
+      int stages, units;
+      if (ctas == 2) {
+        stages = o.stages ? o.stages : tc2_max_stages(bn, d.smem_optin);
+        if (stages == 0 || !tc2_config_supported(bn, stages) ||
+            tc2_smem_bytes(bn, stages) > d.smem_optin)
+          continue;
+        const long long tiles = static_cast<long long>((M + 255) / 256) * ((N + bn - 1) / bn);
+        int pairs = 0;
+        if (tc2_max_active_pairs(bn, stages, d.sm_count & ~1, &pairs) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        pairs = std::min(pairs, d.sm_count / 2);
+        if (pairs <= 0) continue;
+        units = static_cast<int>(std::min<long long>(tiles, pairs));
+        const long long waves = (tiles + pairs - 1) / pairs;
+        const double cost = static_cast<double>(waves) * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
+        if (cost < best - 1e-9) {
+          best = cost;
+          pick = TcConfig{2, bn, stages, false, 2 * units, 16};
+        }
+      } else {
+        stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
+        if (stages == 0 || !tc_config_supported(bn, stages, realign) ||
+            tc_smem_bytes(bn, stages, realign) > d.smem_optin)
+          continue;
+        const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + bn - 1) / bn);
+        units = static_cast<int>(std::min<long long>(tiles, d.sm_count));
+        const long long waves = (tiles + d.sm_count - 1) / d.sm_count;
+        const double cost =
+            1.3 * static_cast<double>(waves) * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
+        if (cost < best - 1e-9) {
+          best = cost;
+          pick = TcConfig{1, bn, stages, realign, units, 16};
+        }
+      }
     }
   }
-  if (!best_bn) return FP8GEMM_EUNSUPPORTED;
-  const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + best_bn - 1) / best_bn);
-  out->bn = best_bn;
-  out->stages = best_stages;
-  out->realign = realign;
-  out->grid = static_cast<int>(std::min<long long>(tiles, d.sm_count));
-  out->group_m = 16;
+  if (!pick.bn) return FP8GEMM_EUNSUPPORTED;
+  *out = pick;
   return FP8GEMM_OK;
 }
 
@@ -240,8 +272,7 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
   fp8gemm_options o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
-  for (int r : o.reserved)
-    if (r != 0) return FP8GEMM_EINVAL;
+  if (o.reserved != 0 || o.mma_ctas < 0 || o.mma_ctas > 2) return FP8GEMM_EINVAL;
   std::memset(pl, 0, sizeof(*pl));
   if (M == 0 || N == 0) return FP8GEMM_OK;  // nothing to do
   const bool tma_ok = (K % 16 == 0) && (!x || aligned16(x)) && (!w || aligned16(w));
@@ -269,25 +300,24 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
   if (path == FP8GEMM_PATH_MAIN) {
     int st = choose_tc(d, M, N, realign, o, &pl->tc);
     if (st != FP8GEMM_OK) return st;
-    int occ = 0;
-    if (tc_blocks_per_sm(pl->tc.bn, pl->tc.stages, realign, &occ) != cudaSuccess) {
-      cudaGetLastError();
-      occ = 0;
-    }
-    pl->pub.tile_m = 128;
+    const bool pair = pl->tc.ctas == 2;
+    pl->pub.tile_m = pair ? 256 : 128;
     pl->pub.tile_n = pl->tc.bn;
     pl->pub.stages = pl->tc.stages;
     pl->pub.splits = 1;
     pl->pub.grid = pl->tc.grid;
-    pl->pub.cluster = 1;
-    pl->pub.threads = tc_threads(realign);
-    pl->pub.smem_bytes = tc_smem_bytes(pl->tc.bn, pl->tc.stages, realign);
-    pl->pub.occupancy = occ;
+    pl->pub.cluster = pair ? 2 : 1;
+    pl->pub.threads = pair ? tc2_threads() : tc_threads(realign);
+    pl->pub.smem_bytes = pair ? tc2_smem_bytes(pl->tc.bn, pl->tc.stages)
+                              : tc_smem_bytes(pl->tc.bn, pl->tc.stages, realign);
+    pl->pub.occupancy = 1;  // one CTA per SM: the ring fills shared memory
     return FP8GEMM_OK;
   }
 
-  // decode path: pick (stages, splits) so that all CTAs are resident in as
-  // few waves as possible and each CTA streams as few K blocks as possible
+  // decode path: one cluster of `s` CTAs per 128-row n-tile, each CTA
+  // streaming ceil(num_kb / s) K blocks.  How many clusters can be resident
+  // at once is limited by cluster placement (CTAs of a cluster share a GPC),
+  // not only by per-SM resources, so it is queried for each candidate.
   if (M > 128) return FP8GEMM_EUNSUPPORTED;
   const int num_kb = (K + 127) / 128;
   const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
@@ -299,16 +329,22 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
     if (!dec_config_supported(mp, stages, realign)) continue;
     const int occ = dec_occupancy(d, mp, stages, realign);
     if (occ <= 0) continue;
-    const long long slots = static_cast<long long>(occ) * d.sm_count;
     const int s_max = std::max(1, std::min(8, num_kb));
     for (int s = 1; s <= s_max; ++s) {
       if (o.splits && s != o.splits) continue;
-      const long long ctas = static_cast<long long>(n_tiles) * s;
-      const long long waves = (ctas + slots - 1) / slots;
+      int clusters = 0;
+      if (dec_max_active_clusters(mp, stages, realign, s, n_tiles * s, &clusters) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (clusters <= 0) continue;
+      const long long waves = (n_tiles + clusters - 1) / clusters;
       const int per_cta = (num_kb + s - 1) / s;
-      // a wave costs its longest CTA; shallow pipelines cost a little more
+      // a wave costs its longest CTA plus a fixed start/reduce cost that grows
+      // with the cluster; shallow rings expose more latency
       const double cost =
-          static_cast<double>(waves) * (std::max(per_cta, 1) + 0.5 + 2.0 / stages);
+          static_cast<double>(waves) * (std::max(per_cta, 1) + 3.0 + 0.5 * s + 8.0 / stages);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best_s = s;
@@ -375,10 +411,12 @@ int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* w
   const bool use_tma = !pl.pub.realign && Ka > 0;
   cudaError_t e;
   if (pl.pub.path == FP8GEMM_PATH_MAIN) {
+    // each CTA of a pair loads 128 rows of x and half of the tile's w rows
+    const int b_rows = pl.tc.ctas == 2 ? pl.tc.bn / 2 : pl.tc.bn;
     if (use_tma && (encode_operand(&tmA, xa, M, Ka, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, wa, N, Ka, pl.tc.bn) != FP8GEMM_OK))
+                    encode_operand(&tmB, wa, N, Ka, b_rows) != FP8GEMM_OK))
       return FP8GEMM_ELAUNCH;
-    e = launch_tc(tmA, tmB, a, pl.tc, s);
+    e = pl.tc.ctas == 2 ? launch_tc2(tmA, tmB, a, pl.tc, s) : launch_tc(tmA, tmB, a, pl.tc, s);
   } else {
     if (use_tma && (encode_operand(&tmA, wa, N, Ka, 128) != FP8GEMM_OK ||
                     encode_operand(&tmB, xa, M, Ka, pl.dec.mp) != FP8GEMM_OK))
@@ -490,9 +528,9 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   r.wo = ws + pl.w_off;
   r.K = K;
   r.Kp = pl.Kp;
-  r.chunks_x = static_cast<long long>(M) * (pl.Kp / 16);
-  r.chunks_w = static_cast<long long>(N) * (pl.Kp / 16);
-  if (launch_repitch(r, d->sm_count, s) != cudaSuccess) {
+  r.rows_x = M;
+  r.rows_w = N;
+  if (launch_repitch(r, s) != cudaSuccess) {
     cudaGetLastError();
     st = FP8GEMM_ELAUNCH;
   } else {
@@ -553,9 +591,9 @@ extern "C" int fp8_gemm_scaled_noalloc(const void* x, const void* w, const float
   r.wo = ws + pl.w_off;
   r.K = K;
   r.Kp = pl.Kp;
-  r.chunks_x = static_cast<long long>(M) * (pl.Kp / 16);
-  r.chunks_w = static_cast<long long>(N) * (pl.Kp / 16);
-  if (launch_repitch(r, d->sm_count, s) != cudaSuccess) {
+  r.rows_x = M;
+  r.rows_w = N;
+  if (launch_repitch(r, s) != cudaSuccess) {
     cudaGetLastError();
     return FP8GEMM_ELAUNCH;
   }

@@ -36,8 +36,15 @@ constexpr int kMmaWarp = 4;
 constexpr int kThreads = 160;
 
 template <int MP>
-constexpr int tmem_cols_for() {
+__host__ __device__ constexpr int tmem_cols_for() {
   return MP <= 32 ? 32 : (MP <= 64 ? 64 : (MP <= 128 ? 128 : 256));
+}
+
+// TMA-issuing warps of the decode producer: the largest divisor of the ring
+// depth that is at most 4, so that every stage has exactly one owner.
+template <int STAGES>
+__host__ __device__ constexpr int issuers_for() {
+  return STAGES % 4 == 0 ? 4 : (STAGES % 3 == 0 ? 3 : (STAGES % 2 == 0 ? 2 : 1));
 }
 
 template <int MP, int STAGES, bool REALIGN>
@@ -55,19 +62,6 @@ struct DCfg {
   static constexpr int kTmemCols = tmem_cols_for<MP>();
   static_assert(MP % 32 == 0 && MP >= 32 && MP <= 128, "MP");
 };
-
-__device__ __noinline__ bool drain_wait_d(uint32_t bar, uint32_t parity, unsigned* err,
-                                          uint64_t budget_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u && globaltimer_ns() - t0 > budget_ns) {
-      atomicOr(err, kErrWaitDrain);
-      return false;
-    }
-  }
-}
 
 template <int MP, int STAGES, bool REALIGN>
 __global__ void __launch_bounds__(kThreads)
@@ -117,7 +111,7 @@ __global__ void __launch_bounds__(kThreads)
     tmem_alloc(holder_addr, C::kTmemCols);
     tmem_relinquish();
   }
-  if (!REALIGN && threadIdx.x == 0) {
+  if (!REALIGN && lane == 0 && warp < 4) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
@@ -130,27 +124,28 @@ __global__ void __launch_bounds__(kThreads)
   if (warp < 4) {
     // ------------------------------------------------------------ producer
     if (!REALIGN) {
-      if (threadIdx.x == 0) {
+      // Stage s is filled by warp s % kIssuers (lane 0): a single issuing
+      // thread cannot keep enough TMA copies in flight to stream the weight.
+      // Each stage has one owner, which therefore reuses it in order.
+      constexpr int kIssuers = issuers_for<STAGES>();
+      if (lane == 0 && static_cast<int>(warp) < kIssuers) {
         const uint64_t pol_stream = l2_policy_evict_first();
         const uint64_t pol_keep = l2_policy_evict_last();
-        uint32_t stage = 0, phase = 0, issued = 0;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) break;
+        int last_use[STAGES];
+        for (int s = 0; s < STAGES; ++s) last_use[s] = -1;
+        for (int i = static_cast<int>(warp); i < my_kb; i += kIssuers) {
+          const int stage = i % STAGES;
+          const uint32_t use = static_cast<uint32_t>(i / STAGES);
+          if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) break;
           mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          const int kb = kb_begin + i;
           tma_load_2d_hint(sA(stage), &tmW, full_bar(stage), kb * kBK, n0, pol_stream);
           tma_load_2d_hint(sB(stage), &tmX, full_bar(stage), kb * kBK, 0, pol_keep);
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          last_use[stage] = static_cast<int>(use);
         }
-        for (int s = 0; s < STAGES; ++s) {
-          if (issued > static_cast<uint32_t>(s)) {
-            const uint32_t n_s = (issued - 1u - s) / STAGES + 1u;
-            drain_wait_d(full_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
-          }
-        }
+        for (int s = 0; s < STAGES; ++s)
+          if (last_use[s] >= 0)
+            drain_wait(full_bar(s), static_cast<uint32_t>(last_use[s]) & 1u, p.err, p.budget_ns);
       }
       __syncwarp();
     } else {
@@ -219,7 +214,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       if (ok && my_kb > 0) tc_commit(acc_full_bar);
       tc_commit(mma_done_bar);
-      drain_wait_d(mma_done_bar, 0u, p.err, p.budget_ns);
+      drain_wait(mma_done_bar, 0u, p.err, p.budget_ns);
     }
     __syncwarp();
   }
@@ -295,10 +290,11 @@ DEntry make_dentry() {
 
 const DEntry kDEntries[] = {
     make_dentry<32, 2, false>(),  make_dentry<32, 3, false>(),  make_dentry<32, 4, false>(),
-    make_dentry<32, 6, false>(),  make_dentry<64, 2, false>(),  make_dentry<64, 3, false>(),
-    make_dentry<64, 4, false>(),  make_dentry<128, 2, false>(), make_dentry<128, 4, false>(),
-    make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),   make_dentry<64, 3, true>(),
-    make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
+    make_dentry<32, 6, false>(),  make_dentry<32, 8, false>(),  make_dentry<32, 10, false>(),
+    make_dentry<64, 2, false>(),  make_dentry<64, 3, false>(),  make_dentry<64, 4, false>(),
+    make_dentry<64, 6, false>(),  make_dentry<64, 8, false>(),  make_dentry<128, 2, false>(),
+    make_dentry<128, 4, false>(), make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),
+    make_dentry<64, 3, true>(),   make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
 };
 
 const DEntry* dfind(int mp, int stages, bool realign) {
@@ -328,14 +324,31 @@ cudaError_t dec_prepare(int mp, int stages, bool realign) {
   cudaError_t r =
       cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
   if (r != cudaSuccess) return r;
-  return cudaSuccess;
+  // several decode CTAs share an SM: ask for the largest shared-memory
+  // carveout, or the SM may be configured with room for only one of them
+  return cudaFuncSetAttribute(e->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
+// Resident CTAs per SM, counted from the kernel's resources: shared memory
+// (228 KB per SM, 1 KB of it reserved per CTA), registers (allocated per warp
+// in units of 256), threads (2048 per SM) and the 32-CTA limit.
 cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out) {
   const DEntry* e = dfind(mp, stages, realign);
   if (!e) return cudaErrorInvalidValue;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, e->fn, kThreads,
-                                                       static_cast<size_t>(e->smem));
+  cudaFuncAttributes fa;
+  cudaError_t r = cudaFuncGetAttributes(&fa, e->fn);
+  if (r != cudaSuccess) return r;
+  const int smem = e->smem + static_cast<int>(fa.sharedSizeBytes) + 1024;
+  const int by_smem = 233472 / smem;
+  const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  const int warps = kThreads / 32;
+  const int by_regs = regs_per_warp > 0 ? 65536 / (warps * regs_per_warp) : 32;
+  const int by_threads = 2048 / kThreads;
+  int n = by_smem < by_regs ? by_smem : by_regs;
+  n = n < by_threads ? n : by_threads;
+  *out = n < 32 ? n : 32;
+  return cudaSuccess;
 }
 
 cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,

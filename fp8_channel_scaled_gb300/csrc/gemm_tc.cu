@@ -12,9 +12,11 @@
 //              TMEM lanes 32w..32w+31 = tile rows), * scale[n], cvt.rn to
 //              bf16, 16-byte global stores
 //   warp  4    TMEM allocator + single-thread tcgen05.mma issuer
-//   warp  5    TMA producer (one thread) -- or, with `realign`, warps 5-8
-//              load rows whose pitch is not a multiple of 16 bytes and
-//              write them into the swizzled layout themselves
+//   warps 5-6  TMA producers, one thread each (warp 5: x tiles, warp 6: w
+//              tiles; one issuing thread alone cannot keep enough copies in
+//              flight) -- or, with `realign`, warps 5-8 load rows whose pitch
+//              is not a multiple of 16 bytes and write them into the
+//              swizzled layout themselves
 //
 // Tile 128 x BN x 128 bytes of K per stage; the accumulator is double
 // buffered in TMEM (2 x BN fp32 columns), so the epilogue of one tile runs
@@ -30,6 +32,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "realign.cuh"
+#include "sched.cuh"
 
 namespace fp8g {
 namespace {
@@ -46,7 +49,7 @@ struct Cfg {
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kProdWarps = REALIGN ? 4 : 1;
+  static constexpr int kProdWarps = REALIGN ? 4 : 2;
   static constexpr int kThreads = 32 * (kProdWarp0 + kProdWarps);
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
   static constexpr int kBarOff = STAGES * kStageBytes;
@@ -57,32 +60,6 @@ struct Cfg {
   static_assert(2 * BN <= kTmemCols, "two accumulators must fit in TMEM");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
-
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mb,
-                                            int& nb) {
-  const int per_group = group_m * num_n;
-  const int g = t / per_group;
-  const int first_m = g * group_m;
-  const int gsize = min(num_m - first_m, group_m);
-  const int r = t - g * per_group;
-  mb = first_m + r % gsize;
-  nb = r / gsize;
-}
-
-// A wait used during teardown: ignores the abort flag (it must wait for work
-// already in flight) but is still bounded.
-__device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned* err,
-                                        uint64_t budget_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u && globaltimer_ns() - t0 > budget_ns) {
-      atomicOr(err, kErrWaitDrain);
-      return false;
-    }
-  }
-}
 
 template <int BN, int STAGES, bool REALIGN>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
@@ -112,7 +89,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), REALIGN ? 32u * C::kProdWarps : 1u);
+      mbar_init(full_bar(s), REALIGN ? 32u * C::kProdWarps : 2u);
       mbar_init(empty_bar(s), 1u);
     }
     for (int a = 0; a < 2; ++a) {
@@ -127,10 +104,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
     tmem_alloc(holder_addr, C::kTmemCols);
     tmem_relinquish();
   }
-  if (!REALIGN && warp == kProdWarp0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
+  if (!REALIGN && warp == kProdWarp0 && lane == 0) tma_prefetch_desc(&tmA);
+  if (!REALIGN && warp == kProdWarp0 + 1 && lane == 0) tma_prefetch_desc(&tmB);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -144,19 +119,24 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
     // ------------------------------------------------------------ producer
     if (!REALIGN) {
       if (lane == 0) {
+        const bool is_a = warp == kProdWarp0;
+        const CUtensorMap* map = is_a ? &tmA : &tmB;
+        const uint32_t bytes = is_a ? C::kABytes : C::kBBytes;
+        const uint32_t off = is_a ? 0u : static_cast<uint32_t>(C::kABytes);
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
           int mb, nb;
           tile_coords(t, num_m_blk, num_n_blk, group_m, mb, nb);
+          const int row = is_a ? mb * kBM : nb * BN;
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-            tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, mb * kBM);
-            tma_load_2d(sB(stage), &tmB, full_bar(stage), kb * kBK, nb * BN);
+            mbar_arrive_expect_tx(full_bar(stage), bytes);
+            tma_load_2d(sbase + static_cast<uint32_t>(stage * C::kStageBytes) + off, map,
+                        full_bar(stage), kb * kBK, row);
             ++issued;
             if (++stage == STAGES) {
               stage = 0;
@@ -342,7 +322,7 @@ int tc_smem_bytes(int bn, int stages, bool realign) {
   return e ? e->smem : -1;
 }
 
-int tc_threads(bool realign) { return 32 * (kProdWarp0 + (realign ? 4 : 1)); }
+int tc_threads(bool realign) { return 32 * (kProdWarp0 + (realign ? 4 : 2)); }
 
 int tc_max_stages(int bn, bool realign, int smem_optin) {
   int best = 0;

@@ -1,0 +1,354 @@
+// gemm_tc2.cu -- persistent tcgen05 kernel on CTA pairs (cta_group::2) for
+// the scaled FP8 linear layer  y = bf16((x_e4m3 . w_e4m3^T, fp32 acc) * scale[n]).
+//
+// The pages' fastest Blackwell submission runs CUTLASS's two-SM UMMA tiles
+// (256 x 256 x 128) for the large shapes ("claude-fable-5" page, CUTLASS 4.0
+// SM100 paragraph).  This kernel is that idea written directly in PTX: a
+// 2-CTA cluster owns a 256 x BN output tile; CTA r (r = 0, 1) loads x rows
+// [256 mb + 128 r, +128) and w rows [BN nb + BN/2 r, +BN/2) of every 128-byte
+// K block into its own shared memory, and the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256), which reads A and B from both CTAs and
+// leaves accumulator rows 0-127 in CTA 0's TMEM and rows 128-255 in CTA 1's.
+// Per SM this halves the B bytes held in shared memory and read by the
+// tensor core, which is what limits the one-CTA 128-row tile.
+//
+// Roles per CTA: warps 0-3 epilogue (TMEM -> * scale -> bf16 -> global),
+// warp 4 TMEM allocation (both CTAs) and MMA issue (even CTA, one thread),
+// warp 5 TMA producer of x, warp 6 TMA producer of w (one thread each: a
+// single issuing thread cannot keep enough TMA copies going to feed the
+// tensor cores, two can).  Synchronisation:
+//   full[s]   in CTA 0 only: CTA 0's two producers arm it, each with its
+//             operand's bytes for both CTAs; both CTAs' loads complete on it;
+//   empty[s]  in both CTAs: the MMA commit multicasts to both;
+//   tfull[a]  in both CTAs: multicast commit after a tile's last K block;
+//   tempty[a] in CTA 0 only: all 8 epilogue warps of the pair arrive on it.
+// Every wait is bounded, as in the one-CTA kernel.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace fp8g {
+namespace {
+
+constexpr int kBK = 128;
+constexpr int kMmaK = 32;
+constexpr int kEpiWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kProdWarpA = 5;   // x rows
+constexpr int kProdWarpB = 6;   // w rows
+constexpr int kThreads = 224;
+
+template <int BN, int STAGES>
+struct Cfg2 {
+  static constexpr int kABytes = 128 * kBK;        // this CTA's 128 rows of x
+  static constexpr int kBRows = BN / 2;            // this CTA's rows of w
+  static constexpr int kBBytes = kBRows * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
+  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(kBRows % 8 == 0, "B half must be whole 8-row swizzle atoms");
+  static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_linear_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
+                          const int num_m2_blk, const int num_n_blk, const int group_m) {
+  using C = Cfg2<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+
+  const uint32_t bar0 = sbase + C::kBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 4);
+  const uint32_t holder_addr = bar0 + 8u * C::kNumBars;
+  volatile uint32_t* holder =
+      reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOff + 8 * C::kNumBars);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(gbase + C::kBarOff + 8 * C::kNumBars + 4);
+  auto sA = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes); };
+  auto sB = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes + C::kABytes); };
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();  // 0 = even CTA (MMA issuer), 1 = its peer
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 2u);  // the two producers of CTA 0
+      mbar_init(empty_bar(s), 1u);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1u);
+      mbar_init(tempty_bar(a), static_cast<uint32_t>(2 * kEpiWarps));
+    }
+    mbar_init(mma_done_bar, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(holder_addr, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == kProdWarpA && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == kProdWarpB && lane == 0) tma_prefetch_desc(&tmB);
+  // both CTAs' barriers are initialised (and TMEM allocated) before any
+  // cross-CTA arrive or TMA completion
+  tc_fence_before_sync();
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *holder;
+
+  const WaitCtx wc{p.err, abort_flag, p.budget_ns};
+  const int num_tiles = num_m2_blk * num_n_blk;
+  const int num_kb = p.num_kb;
+
+  if (warp == kProdWarpA || warp == kProdWarpB) {
+    // ------------------------------------------------------------ producers
+    if (lane == 0) {
+      const bool is_a = warp == kProdWarpA;
+      const CUtensorMap* map = is_a ? &tmA : &tmB;
+      const uint32_t bytes = is_a ? C::kABytes : C::kBBytes;
+      const uint32_t off = is_a ? 0u : static_cast<uint32_t>(C::kABytes);
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+        int mb, nb;
+        tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
+        const int row = is_a ? mb * 256 + static_cast<int>(rank) * 128
+                             : nb * BN + static_cast<int>(rank) * C::kBRows;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+          tma_load_2d_pair(sbase + static_cast<uint32_t>(stage * C::kStageBytes) + off, map,
+                           mapa_shared(full_bar(stage), 0u), kb * kBK, row);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Teardown: every load issued must have landed.  CTA 0 sees its full
+      // barriers complete; CTA 1's loads complete on CTA 0's barrier, so it
+      // waits for the MMA release of each stage it filled last instead.
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued > static_cast<uint32_t>(s)) {
+          const uint32_t n_s = (issued - 1u - s) / STAGES + 1u;
+          if (rank == 0)
+            drain_wait(full_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
+          else
+            drain_wait(empty_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t kIdesc = idesc_e4m3_f32(256, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wc, kErrWaitMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, wc, kErrWaitMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
+          const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
+#pragma unroll
+          for (int k = 0; k < kBK / kMmaK; ++k)
+            tc_mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, kIdesc,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          tc_commit_pair_mc(empty_bar(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull_bar(acc), 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit_pair_mc(mma_done_bar, 0x1);
+      drain_wait(mma_done_bar, 0u, p.err, p.budget_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    uint32_t acc = 0, acc_phase = 0;
+    const bool zero_acc = (num_kb == 0);
+    for (int t = pair; t < num_tiles; t += num_pairs) {
+      int mb, nb;
+      tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
+      tc_fence_after_sync();
+      const int row = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32 +
+                      static_cast<int>(lane);
+      const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
+      uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, v);
+        tmem_ld_wait();
+        const int col0 = nb * BN + c * 32;
+        const float sc =
+            (col0 + static_cast<int>(lane) < p.N) ? __ldg(p.scale + col0 + lane) : 0.f;
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+          const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+          const float a0 = zero_acc ? 0.f : __uint_as_float(v[2 * j]);
+          const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
+          packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
+        }
+        if (row < p.M) {
+          if (p.vec_store && col0 + 32 <= p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                  packed[4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < p.N)
+                yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
+                                                               : (packed[j >> 1] & 0xFFFFu));
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0u));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  // The even CTA's MMAs (which write both CTAs' TMEM) are complete and every
+  // epilogue has read its accumulators before the pair frees TMEM together.
+  tc_fence_before_sync();
+  cluster_sync_all();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ dispatch
+struct Entry2 {
+  int bn, stages;
+  const void* fn;
+  int smem;
+};
+
+template <int BN, int S>
+Entry2 make_entry2() {
+  return Entry2{BN, S, reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S>),
+                Cfg2<BN, S>::kSmemBytes};
+}
+
+const Entry2 kEntries2[] = {
+    make_entry2<256, 6>(), make_entry2<256, 7>(), make_entry2<224, 7>(), make_entry2<192, 8>(),
+    make_entry2<160, 8>(), make_entry2<128, 8>(),
+};
+
+const Entry2* find2(int bn, int stages) {
+  for (const Entry2& e : kEntries2)
+    if (e.bn == bn && e.stages == stages) return &e;
+  return nullptr;
+}
+
+}  // namespace
+
+bool tc2_config_supported(int bn, int stages) { return find2(bn, stages) != nullptr; }
+
+int tc2_smem_bytes(int bn, int stages) {
+  const Entry2* e = find2(bn, stages);
+  return e ? e->smem : -1;
+}
+
+int tc2_threads() { return kThreads; }
+
+int tc2_max_stages(int bn, int smem_optin) {
+  int best = 0;
+  for (const Entry2& e : kEntries2)
+    if (e.bn == bn && e.smem <= smem_optin && e.stages > best) best = e.stages;
+  return best;
+}
+
+cudaError_t tc2_prepare(int bn, int stages) {
+  const Entry2* e = find2(bn, stages);
+  if (!e) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
+}
+
+cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out) {
+  const Entry2* e = find2(bn, stages);
+  if (!e) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, e->fn, &cfg);
+}
+
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                       const TcConfig& c, cudaStream_t s) {
+  const Entry2* e = find2(c.bn, c.stages);
+  if (!e || c.grid % 2) return cudaErrorInvalidValue;
+  const int num_m2 = (a.M + 255) / 256;
+  const int num_n = (a.N + c.bn - 1) / c.bn;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  CUtensorMap mA = tmA, mB = tmB;
+  GemmArgs args = a;
+  int m2 = num_m2, nn = num_n, gm = c.group_m;
+  void* params[] = {&mA, &mB, &args, &m2, &nn, &gm};
+  return cudaLaunchKernelExC(&cfg, e->fn, params);
+}
+
+}  // namespace fp8g

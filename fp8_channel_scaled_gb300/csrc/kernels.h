@@ -24,7 +24,8 @@ struct GemmArgs {
 
 // ---- persistent tcgen05 kernel (large M) ---------------------------------
 struct TcConfig {
-  int bn;          // N tile (128 or 256); the M tile is 128, the K block 128 bytes
+  int ctas;        // 1: one-CTA 128-row tiles; 2: CTA-pair 256-row tiles (gemm_tc2.cu)
+  int bn;          // N tile; the K block is 128 bytes
   int stages;      // shared-memory pipeline depth
   bool realign;    // operands loaded by the realigning producer instead of TMA
   int grid;        // persistent CTAs
@@ -38,6 +39,16 @@ cudaError_t tc_prepare(int bn, int stages, bool realign);  // per device, before
 cudaError_t tc_blocks_per_sm(int bn, int stages, bool realign, int* out);
 cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                       const TcConfig& c, cudaStream_t s);
+
+// ---- persistent tcgen05 kernel on CTA pairs (large M) -----------------------
+bool tc2_config_supported(int bn, int stages);
+int tc2_smem_bytes(int bn, int stages);
+int tc2_threads();
+int tc2_max_stages(int bn, int smem_optin);
+cudaError_t tc2_prepare(int bn, int stages);
+cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out);
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                       const TcConfig& c, cudaStream_t s);
 
 // ---- split-K decode kernel (small M, swap-AB, cluster reduce) -------------
 struct DecConfig {
@@ -66,9 +77,9 @@ struct RepitchArgs {
   uint8_t* xo;           // [M, Kp], 16-byte aligned
   uint8_t* wo;           // [N, Kp], 16-byte aligned
   int K, Kp;             // Kp = round_up(K, 16)
-  long long chunks_x;    // M * Kp / 16
-  long long chunks_w;    // N * Kp / 16
+  long long rows_x;      // M
+  long long rows_w;      // N
 };
-cudaError_t launch_repitch(const RepitchArgs& a, int sm_count, cudaStream_t s);
+cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s);
 
 }  // namespace fp8g

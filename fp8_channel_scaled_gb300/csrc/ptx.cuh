@@ -80,22 +80,47 @@ struct WaitCtx {
   uint64_t budget_ns;        // longest single wait
 };
 
-// Wait until the phase of `bar` with parity `parity` has completed.  Returns
-// false (and records `code`) if it did not complete within the budget or if
-// another wait of this CTA already gave up.  Never waits without limit.
-static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& wc,
-                                               unsigned code) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait_bounded (scalar arguments, so the call needs no
+// stack frame).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned* err,
+                                                   volatile int* abort_flag, uint64_t budget_ns,
+                                                   unsigned code) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
-      if (*wc.abort_flag) return false;
-      if (globaltimer_ns() - t0 > wc.budget_ns) {
-        *wc.abort_flag = 1;
-        atomicOr(wc.err, code);
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > budget_ns) {
+        *abort_flag = 1;
+        atomicOr(err, code);
         return false;
       }
+    }
+  }
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed.  Returns
+// false (and records `code`) if it did not complete within the budget or if
+// another wait of this CTA already gave up.  Never waits without limit.  The
+// common case (phase already complete, or completing within one try_wait
+// suspension) stays inline.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const WaitCtx& wc, unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, wc.err, wc.abort_flag, wc.budget_ns, code);
+}
+
+// A wait used during teardown: ignores the abort flag (it must wait for work
+// already in flight) but is still bounded.
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                               uint64_t budget_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u && globaltimer_ns() - t0 > budget_ns) {
+      atomicOr(err, kErrWaitDrain);
+      return false;
     }
   }
 }
@@ -265,6 +290,67 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05 on a CTA pair (cta_group::2): the even CTA of a 2-CTA cluster issues
+// MMAs whose A rows and B rows are split between the two CTAs' shared memory
+// (same offsets) and whose accumulator rows live in both CTAs' TMEM.
+// ----------------------------------------------------------------------------
+// Collective: one warp in each CTA of the pair executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+// Collective: one warp in each CTA of the pair executes it.
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D (both CTAs' TMEM) (+)= A (rows split over the pair) * B^T (rows split over
+// the pair); M = 256, issued by one thread of the even CTA.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at this shared-memory offset in every CTA of
+// `cta_mask` when all pair MMAs this thread issued have completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Arrive on an mbarrier given by its cluster address (possibly another CTA's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
 }
 
 // ----------------------------------------------------------------------------

@@ -13,7 +13,7 @@
 // One thread produces one aligned 16-byte output chunk from the (at most)
 // two aligned 16-byte source words that hold it, so loads and stores are
 // both 16 bytes wide and coalesced along the row; each thread keeps four
-// chunks in flight.  No load touches a 16-byte word that holds no byte of
+// chunks in flight.  A row holds at most 2^31 / 16 chunks (K < 2^31).  No load touches a 16-byte word that holds no byte of
 // the operand.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -24,40 +24,40 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kIlp = 4;
+constexpr int kRowsPerBlock = 8;
 
-__device__ __forceinline__ void chunk_of(const RepitchArgs& a, long long u, const uint8_t*& src,
-                                         uint8_t*& dst, int& valid) {
-  const long long cpr = a.Kp / 16;
-  const bool is_w = u >= a.chunks_x;
-  const long long v = is_w ? u - a.chunks_x : u;
-  const long long r = v / cpr;
-  const int c = static_cast<int>(v - r * cpr);
-  const int kc = 16 * c;
-  src = (is_w ? a.w : a.x) + r * a.K + kc;
-  dst = (is_w ? a.wo : a.xo) + r * a.Kp + kc;
-  valid = min(16, a.K - kc);
-}
-
+// Each block copies kRowsPerBlock consecutive rows of the stacked [x; w]
+// matrix (M + N rows); its threads walk the rows' 16-byte output chunks with
+// block-local 32-bit indices, kIlp chunks in flight per thread.
 __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) {
-  const long long total = a.chunks_x + a.chunks_w;
-  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
-  for (long long base = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; base < total;
-       base += stride * kIlp) {
+  const int cpr = a.Kp / 16;  // chunks per row
+  const long long row0 = static_cast<long long>(blockIdx.x) * kRowsPerBlock;
+  const long long rows_total = a.rows_x + a.rows_w;
+  const long long left = rows_total - row0;
+  const int rows_here = left < kRowsPerBlock ? static_cast<int>(left) : kRowsPerBlock;
+  const int units = rows_here * cpr;
+  for (int base = static_cast<int>(threadIdx.x); base < units; base += kThreads * kIlp) {
     uint4 lo[kIlp], hi[kIlp];
     uint32_t sh[kIlp];
     int valid[kIlp];
     uint8_t* dst[kIlp];
 #pragma unroll
     for (int i = 0; i < kIlp; ++i) {
-      const long long u = base + i * stride;
+      const int u = base + i * kThreads;
       lo[i] = make_uint4(0, 0, 0, 0);
       hi[i] = make_uint4(0, 0, 0, 0);
       sh[i] = 0;
       valid[i] = 0;
       dst[i] = nullptr;
-      if (u < total) {
-        const uint8_t* src;
-        chunk_of(a, u, src, dst[i], valid[i]);
+      if (u < units) {
+        const int rl = u / cpr;
+        const int kc = 16 * (u - rl * cpr);
+        const long long r = row0 + rl;
+        const bool is_w = r >= a.rows_x;
+        const long long rr = is_w ? r - a.rows_x : r;
+        const uint8_t* src = (is_w ? a.w : a.x) + rr * a.K + kc;
+        dst[i] = (is_w ? a.wo : a.xo) + rr * a.Kp + kc;
+        valid[i] = min(16, a.K - kc);
         sh[i] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
         const uint8_t* w0 = src - sh[i];
         lo[i] = ldg_nc_v4(w0);
@@ -76,13 +76,11 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) 
 
 }  // namespace
 
-cudaError_t launch_repitch(const RepitchArgs& a, int sm_count, cudaStream_t s) {
-  const long long total = a.chunks_x + a.chunks_w;
-  if (total <= 0) return cudaSuccess;
-  long long blocks = (total + static_cast<long long>(kThreads) * kIlp - 1) /
-                     (static_cast<long long>(kThreads) * kIlp);
-  const long long cap = static_cast<long long>(sm_count) * 8;
-  if (blocks > cap) blocks = cap;
+cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
+  const long long rows = a.rows_x + a.rows_w;
+  if (rows <= 0 || a.Kp <= 0) return cudaSuccess;
+  const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   repitch_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -80,7 +80,9 @@ typedef struct {
     int splits;         /* decode path K splits (cluster size): 0 auto, 1..8 */
     int no_workspace;   /* 1: never repitch; rows TMA cannot tile are then
                            loaded by the in-kernel realigning producer */
-    int reserved[2];    /* must be zero */
+    int mma_ctas;       /* main path: 0 auto, 1 one-CTA 128-row tiles,
+                           2 CTA-pair 256-row tiles (tcgen05 cta_group::2) */
+    int reserved;       /* must be zero */
     void *workspace;    /* optional caller workspace (device, 256-byte aligned) */
     size_t workspace_bytes; /* its size; must be >= fp8_gemm_workspace_bytes() */
 } fp8gemm_options;
@@ -89,12 +91,13 @@ typedef struct {
 typedef struct {
     int path;           /* FP8GEMM_PATH_MAIN or FP8GEMM_PATH_DECODE; 0 = no launch */
     int realign;        /* 1: operands loaded by the realigning producer */
-    int tile_m;         /* rows of x per tile (main) / rows of w per tile (decode) */
+    int tile_m;         /* rows of x per tile (main: 128, or 256 on a CTA pair) /
+                           rows of w per tile (decode) */
     int tile_n;         /* columns of y per tile (main) / padded M (decode) */
     int stages;         /* shared-memory pipeline depth */
     int splits;         /* K splits (decode), 1 for main */
     int grid;           /* CTAs launched */
-    int cluster;        /* CTAs per cluster */
+    int cluster;        /* CTAs per cluster (2 for CTA-pair tiles, splits for decode) */
     int threads;        /* threads per CTA */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int launches;       /* kernels launched by one call (0, 1, or 2 with repitch) */

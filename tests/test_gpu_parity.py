@@ -71,15 +71,51 @@ MAIN_SHAPES = [
 
 
 @pytest.mark.parametrize("M,N,K", MAIN_SHAPES)
-def test_main_path_shapes(M, N, K):
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_main_path_shapes(M, N, K, ctas):
     x, w, s = synth.make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-    check_full(x, w, s, Options(path=PATH_MAIN), what=f"main {M}x{N}x{K}")
+    check_full(x, w, s, Options(path=PATH_MAIN, mma_ctas=ctas), what=f"main {M}x{N}x{K} ctas={ctas}")
 
 
 @pytest.mark.parametrize("bn", [128, 160, 192, 224, 256])
 def test_main_path_tiles(bn):
     x, w, s = synth.make_inputs(300, 520, 640, seed=5)
-    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn), what=f"main bn={bn}")
+    check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn, mma_ctas=1), what=f"main bn={bn}")
+
+
+PAIR_SHAPES = [
+    (256, 256, 256), (512, 448, 1024), (257, 300, 520), (129, 136, 128), (1000, 1000, 4096),
+    (300, 257, 17 * 16), (64, 512, 256),
+]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_cta_pair_tiles(M, N, K):
+    x, w, s = synth.make_inputs(M, N, K, seed=M + 3 * N + 7 * K)
+    p = fg.plan(M, N, K, Options(path=PATH_MAIN, mma_ctas=2))
+    assert p.tile_m == 256 and p.cluster == 2 and p.grid % 2 == 0
+    check_full(x, w, s, Options(path=PATH_MAIN, mma_ctas=2), what=f"pair {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bn", [128, 160, 192, 224, 256])
+def test_cta_pair_tile_widths(bn):
+    x, w, s = synth.make_inputs(600, 1000, 640, seed=bn)
+    check_full(x, w, s, Options(path=PATH_MAIN, mma_ctas=2, tile_n=bn), what=f"pair bn={bn}")
+
+
+def test_cta_pair_equals_single_cta_on_exact_sums():
+    # integer operands: every fp32 partial sum is exact, so both tile kinds
+    # must give identical bits (and equal the oracle's)
+    codes = synth.quantize_e4m3(np.arange(-16, 17, dtype=np.float64))
+    rng = np.random.default_rng(9)
+    M, N, K = 384, 448, 2048
+    x = rng.choice(codes, (M, K)).astype(np.uint8)
+    w = rng.choice(codes, (N, K)).astype(np.uint8)
+    s = (2.0 ** -rng.integers(0, 12, N)).astype(np.float32)
+    a = run(x, w, s, Options(path=PATH_MAIN, mma_ctas=2))
+    b = run(x, w, s, Options(path=PATH_MAIN, mma_ctas=1))
+    assert np.array_equal(a, b)
+    assert np.array_equal(a, oracle.linear(x, w, s))
 
 
 @pytest.mark.parametrize("bn", [128, 224, 256])

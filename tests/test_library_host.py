@@ -76,7 +76,7 @@ def test_argument_checks_before_any_cuda_call(cdll):
     # non-zero reserved option fields
     import fp8_channel_scaled_gb300._binding as b
     o = b._COptions()
-    o.reserved[1] = 7
+    o.reserved = 7
     assert cdll.fp8_gemm_plan(0, None, None, 4, 4, 4, ctypes.byref(o), ctypes.byref(b._CPlan())) in (1, 3)
 
 
