@@ -37,10 +37,9 @@ METRIC = "FP8 GEMM TFLOP/s (GB/s at M=32) per config; fraction of GB300 roofline
 HEADLINE = "square"
 FP8_OVER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-TC_SOURCES = ["fp8_channel_scaled_gb300/csrc/gemm_tc.cu", "fp8_channel_scaled_gb300/csrc/ptx.cuh",
-              "fp8_channel_scaled_gb300/csrc/realign.cuh"]
-DEC_SOURCES = ["fp8_channel_scaled_gb300/csrc/gemm_decode.cu",
-               "fp8_channel_scaled_gb300/csrc/ptx.cuh", "fp8_channel_scaled_gb300/csrc/realign.cuh"]
+_CSRC = "fp8_channel_scaled_gb300/csrc/"
+TC_SOURCES = [_CSRC + f for f in ("gemm_tc.cu", "gemm_tc2.cu", "ptx.cuh", "realign.cuh", "sched.cuh")]
+DEC_SOURCES = [_CSRC + f for f in ("gemm_decode.cu", "ptx.cuh", "realign.cuh")]
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -386,7 +385,7 @@ def run_ours(args):
             gbs = wl2.algorithmic_bytes / k2 / 1e9
             roof_t = max(wl2.flops / 4.5e15, wl2.algorithmic_bytes / 8e12)
             p2 = fg.plan(wl2.M, wl2.N, wl2.K, x=sets2[0][0], w=sets2[0][1])
-            others[key] = {"workload": wl2.name, "us_median": round(k2 * 1e6, 2),
+            others[key2] = {"workload": wl2.name, "us_median": round(k2 * 1e6, 2),
                            "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1),
                            "frac_roofline_nominal": round(roof_t / k2, 4),
                            "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
@@ -430,19 +429,24 @@ def run_reference(args):
     wl = synth.WORKLOADS[HEADLINE]
     x, w, s = synth.workload_inputs(HEADLINE)
     cores = oracle.default_threads()
-    t0 = time.perf_counter()
-    oracle.linear_rows(x, w, s, np.arange(cores, dtype=np.int64))
-    per_row = (time.perf_counter() - t0) / cores
-    total = args.steps + args.warmup
-    rows_per_step = int(max(1, min(wl.M, args.cpu_seconds * 4 / max(total, 1) / max(per_row, 1e-9))))
     rng = np.random.default_rng(0)
-    for _ in range(args.warmup):
-        oracle.linear_rows(x, w, s, rng.integers(0, wl.M, rows_per_step))
+    # time per output element, measured on a probe spread over all cores
+    probe = 64 * cores
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.linear_rows(x, w, s, rng.integers(0, wl.M, rows_per_step))
+    oracle.linear_elems(x, w, s, rng.integers(0, wl.M, probe), rng.integers(0, wl.N, probe))
+    per_elem = (time.perf_counter() - t0) / probe
+    # each step is a bounded sample of output elements, sized so that the
+    # whole --steps/--warmup run takes about 4x --cpu-seconds
+    total = args.steps + args.warmup
+    n = int(max(cores, min(wl.M * wl.N, args.cpu_seconds * 4 / max(total, 1) / max(per_elem, 1e-12))))
+    samples = [(rng.integers(0, wl.M, n), rng.integers(0, wl.N, n)) for _ in range(min(total, 8))]
+    for i in range(args.warmup):
+        oracle.linear_elems(x, w, s, *samples[i % len(samples)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.linear_elems(x, w, s, *samples[i % len(samples)])
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows_per_step * wl.N * wl.K * args.steps
+    flops = 2.0 * n * wl.K * args.steps
     value = flops / dt / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -452,7 +456,7 @@ def run_reference(args):
             "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "seed": wl.seed,
                        "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{rows_per_step} random rows of {wl.M} per step (full N, K)"},
+                             "sample": f"{n} random output elements of {wl.M}x{wl.N} per step (full K={wl.K})"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
