@@ -63,7 +63,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> Path:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB.with_name(f"{LIB.name}.tmp{os.getpid()}")
-    cmd = [nv, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", str(tmp), *map(str, objs)]
+    # -z defs: an unresolved symbol fails the build instead of the first load
+    cmd = [nv, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-Xlinker", "-zdefs", "-o", str(tmp),
+           *map(str, objs)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -81,7 +81,7 @@ unsigned long long budget_ns() {
 
 const int kTcTiles[] = {256, 224, 192, 160, 128};
 const int kTcStages[] = {3, 4, 5, 6, 7};
-const int kTc2Stages[] = {6, 7, 8};
+const int kTc2Stages[] = {6, 8};
 const int kDecMp[] = {32, 64, 128};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
@@ -179,6 +179,19 @@ int encode_operand(CUtensorMap* map, const void* base, int rows, int K, int box_
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8GEMM_OK : FP8GEMM_ELAUNCH;
+}
+
+// TMA descriptor of y as bf16 [M, N] for 32 x 32 output boxes with the
+// 64-byte swizzle (requires N % 8 == 0 and a 16-byte aligned y).
+int encode_output(CUtensorMap* map, void* y, int M, int N) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2u};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FP8GEMM_OK : FP8GEMM_ELAUNCH;
 }
 
@@ -416,7 +429,14 @@ int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* w
     if (use_tma && (encode_operand(&tmA, xa, M, Ka, 128) != FP8GEMM_OK ||
                     encode_operand(&tmB, wa, N, Ka, b_rows) != FP8GEMM_OK))
       return FP8GEMM_ELAUNCH;
-    e = pl.tc.ctas == 2 ? launch_tc2(tmA, tmB, a, pl.tc, s) : launch_tc(tmA, tmB, a, pl.tc, s);
+    if (pl.tc.ctas == 2) {
+      CUtensorMap tmY;
+      std::memset(&tmY, 0, sizeof(tmY));
+      if (a.vec_store && encode_output(&tmY, y, M, N) != FP8GEMM_OK) return FP8GEMM_ELAUNCH;
+      e = launch_tc2(tmA, tmB, tmY, a, pl.tc, s);
+    } else {
+      e = launch_tc(tmA, tmB, a, pl.tc, s);
+    }
   } else {
     if (use_tma && (encode_operand(&tmA, wa, N, Ka, 128) != FP8GEMM_OK ||
                     encode_operand(&tmB, xa, M, Ka, pl.dec.mp) != FP8GEMM_OK))

@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after_sync();
+          // TMA data reach the MMA through the full barrier alone; operands written
+          // by producer threads (generic proxy) additionally need the tcgen05 fence
+          if (REALIGN) tc_fence_after_sync();
           const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
           const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
 #pragma unroll

@@ -12,13 +12,15 @@
 // Per SM this halves the B bytes held in shared memory and read by the
 // tensor core, which is what limits the one-CTA 128-row tile.
 //
-// Roles per CTA: warps 0-3 epilogue (TMEM -> * scale -> bf16 -> global),
-// warp 4 TMEM allocation (both CTAs) and MMA issue (even CTA, one thread),
-// warp 5 TMA producer of x, warp 6 TMA producer of w (one thread each: a
-// single issuing thread cannot keep enough TMA copies going to feed the
-// tensor cores, two can).  Synchronisation:
-//   full[s]   in CTA 0 only: CTA 0's two producers arm it, each with its
-//             operand's bytes for both CTAs; both CTAs' loads complete on it;
+// Roles per CTA: warps 0-3 epilogue (TMEM -> * scale -> bf16 -> swizzled
+// shared-memory staging -> TMA store), warp 4 TMEM allocation (both CTAs)
+// and MMA issue (even CTA, one thread), warps 5-8 TMA producers, one thread
+// each: x of even stages, x of odd stages, w of even stages, w of odd stages
+// (a TMA copy keeps its issuing thread busy for hundreds of cycles, so one
+// thread per operand cannot keep the tensor cores fed).  Synchronisation:
+//   full[s]   in CTA 0 only: CTA 0's x and w producers of stage s arm it, each
+//             with its operand's bytes for both CTAs; both CTAs' loads
+//             complete on it;
 //   empty[s]  in both CTAs: the MMA commit multicasts to both;
 //   tfull[a]  in both CTAs: multicast commit after a tile's last K block;
 //   tempty[a] in CTA 0 only: all 8 epilogue warps of the pair arrive on it.
@@ -36,9 +38,9 @@ constexpr int kBK = 128;
 constexpr int kMmaK = 32;
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarpA = 5;   // x rows
-constexpr int kProdWarpB = 6;   // w rows
-constexpr int kThreads = 224;
+constexpr int kProdWarp0 = 5;   // warps 5-8: (x, even), (x, odd), (w, even), (w, odd) stages
+constexpr int kThreads = 288;
+constexpr int kStgBytes = 2048;  // one 32 x 32 bf16 staging box (64-byte swizzle)
 
 template <int BN, int STAGES>
 struct Cfg2 {
@@ -47,19 +49,22 @@ struct Cfg2 {
   static constexpr int kBBytes = kBRows * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
-  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kStgOff = STAGES * kStageBytes;            // 4 warps x 2 staging boxes
+  static constexpr int kBarOff = kStgOff + kEpiWarps * 2 * kStgBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(kBRows % 8 == 0, "B half must be whole 8-row swizzle atoms");
   static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
+  static_assert(STAGES % 2 == 0, "each stage is owned by one x and one w producer");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_linear_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmY, const GemmArgs p,
                           const int num_m2_blk, const int num_n_blk, const int group_m) {
   using C = Cfg2<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -104,8 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(holder_addr, C::kTmemCols);
     tmem_relinquish_pair();
   }
-  if (warp == kProdWarpA && lane == 0) tma_prefetch_desc(&tmA);
-  if (warp == kProdWarpB && lane == 0) tma_prefetch_desc(&tmB);
+  if (warp == kProdWarp0 && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == kProdWarp0 + 2 && lane == 0) tma_prefetch_desc(&tmB);
+  if (warp == 0 && lane == 0 && p.vec_store) tma_prefetch_desc(&tmY);
   // both CTAs' barriers are initialised (and TMEM allocated) before any
   // cross-CTA arrive or TMA completion
   tc_fence_before_sync();
@@ -117,46 +123,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = num_m2_blk * num_n_blk;
   const int num_kb = p.num_kb;
 
-  if (warp == kProdWarpA || warp == kProdWarpB) {
+  if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
-      const bool is_a = warp == kProdWarpA;
+      const uint32_t q = warp - kProdWarp0;
+      const bool is_a = q < 2;
+      const uint32_t parity = q & 1u;  // stages s with s % 2 == parity
       const CUtensorMap* map = is_a ? &tmA : &tmB;
       const uint32_t bytes = is_a ? C::kABytes : C::kBBytes;
       const uint32_t off = is_a ? 0u : static_cast<uint32_t>(C::kABytes);
-      uint32_t stage = 0, phase = 0, issued = 0;
+      uint32_t it = 0;  // (tile, K block) iteration, shared numbering of all producers
       bool ok = true;
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
         int mb, nb;
         tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
         const int row = is_a ? mb * 256 + static_cast<int>(rank) * 128
                              : nb * BN + static_cast<int>(rank) * C::kBRows;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) {
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          if ((it & 1u) != parity) continue;
+          const uint32_t stage = it % STAGES;
+          const uint32_t use = it / STAGES;
+          if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) {
             ok = false;
             break;
           }
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
-          tma_load_2d_pair(sbase + static_cast<uint32_t>(stage * C::kStageBytes) + off, map,
+          tma_load_2d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) + off, map,
                            mapa_shared(full_bar(stage), 0u), kb * kBK, row);
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
       }
-      // Teardown: every load issued must have landed.  CTA 0 sees its full
-      // barriers complete; CTA 1's loads complete on CTA 0's barrier, so it
-      // waits for the MMA release of each stage it filled last instead.
-      for (int s = 0; s < STAGES; ++s) {
-        if (issued > static_cast<uint32_t>(s)) {
-          const uint32_t n_s = (issued - 1u - s) / STAGES + 1u;
-          if (rank == 0)
-            drain_wait(full_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
-          else
-            drain_wait(empty_bar(s), (n_s - 1u) & 1u, p.err, p.budget_ns);
-        }
+      // Teardown: every load this thread issued (iterations < it of its
+      // parity) must have landed.  CTA 0 sees its full barriers complete;
+      // CTA 1's loads complete on CTA 0's barrier, so it waits for the MMA's
+      // release of the stage instead.  Each stage barrier completes exactly
+      // one phase per use, so the last use's parity is unambiguous.
+      for (uint32_t back = 1; back <= STAGES && back <= it; ++back) {
+        const uint32_t i = it - back;
+        if ((i & 1u) != parity) continue;
+        const uint32_t ph = (i / STAGES) & 1u;
+        if (rank == 0)
+          drain_wait(full_bar(i % STAGES), ph, p.err, p.budget_ns);
+        else
+          drain_wait(empty_bar(i % STAGES), ph, p.err, p.budget_ns);
       }
     }
     __syncwarp();
@@ -175,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after_sync();
+          // the TMA bytes reach the MMA through the full barrier alone: no tcgen05
+          // fence per K block (one would hold the issue back until earlier MMAs drain)
           const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
           const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
 #pragma unroll
@@ -199,19 +208,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    uint32_t acc = 0, acc_phase = 0;
+    // Each warp owns 32 accumulator rows.  Per 32-column chunk: TMEM ->
+    // registers, * scale[n], round to bf16, write the 32 x 32 box into one of
+    // two 64-byte-swizzled staging boxes and let one lane TMA-store it (the
+    // store clips rows >= M and columns >= N).  Without a usable y map
+    // (N % 8 != 0 or y not 16-byte aligned) rows are stored directly.
+    uint32_t acc = 0, acc_phase = 0, chunk_no = 0;
     const bool zero_acc = (num_kb == 0);
+    const bool tma_y = p.vec_store != 0;
+    const uint32_t stg = sbase + static_cast<uint32_t>(C::kStgOff) + warp * 2u * kStgBytes;
     for (int t = pair; t < num_tiles; t += num_pairs) {
       int mb, nb;
       tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
       tc_fence_after_sync();
-      const int row = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32 +
-                      static_cast<int>(lane);
+      const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
+      const int row = row0 + static_cast<int>(lane);
       const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
       uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 32; ++c, ++chunk_no) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + c * 32, v);
         tmem_ld_wait();
@@ -227,20 +243,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
           packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
         }
-        if (row < p.M) {
-          if (p.vec_store && col0 + 32 <= p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
+        if (tma_y) {
+          const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
+          if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
+            if (lane == 0) tma_store_wait_read<1>();
+            __syncwarp();
+          }
+          // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
+          const uint32_t rb = buf + lane * 64u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                                  packed[4 * q + 3]);
-          } else {
+          for (int q = 0; q < 4; ++q)
+            sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+                   make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                              packed[4 * q + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // boxes entirely past M or N are not issued; the (possibly empty)
+            // group is committed either way so that the buffer accounting
+            // above always refers to the same chunk
+            if (row0 < p.M && col0 < p.N) tma_store_2d(&tmY, buf, col0, row0);
+            tma_store_commit();
+          }
+        } else if (row < p.M) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < p.N)
-                yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
-                                                               : (packed[j >> 1] & 0xFFFFu));
-            }
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j < p.N)
+              yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
+                                                             : (packed[j >> 1] & 0xFFFFu));
           }
         }
       }
@@ -250,6 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // every store must have finished reading shared memory (and be issued to
+    // global memory) before the CTA exits
+    if (tma_y && lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -275,8 +309,8 @@ Entry2 make_entry2() {
 }
 
 const Entry2 kEntries2[] = {
-    make_entry2<256, 6>(), make_entry2<256, 7>(), make_entry2<224, 7>(), make_entry2<192, 8>(),
-    make_entry2<160, 8>(), make_entry2<128, 8>(),
+    make_entry2<256, 6>(), make_entry2<224, 6>(), make_entry2<192, 6>(), make_entry2<160, 8>(),
+    make_entry2<128, 8>(),
 };
 
 const Entry2* find2(int bn, int stages) {
@@ -326,8 +360,8 @@ cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out) {
   return cudaOccupancyMaxActiveClusters(out, e->fn, &cfg);
 }
 
-cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                       const TcConfig& c, cudaStream_t s) {
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                       const GemmArgs& a, const TcConfig& c, cudaStream_t s) {
   const Entry2* e = find2(c.bn, c.stages);
   if (!e || c.grid % 2) return cudaErrorInvalidValue;
   const int num_m2 = (a.M + 255) / 256;
@@ -344,10 +378,10 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gem
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  CUtensorMap mA = tmA, mB = tmB;
+  CUtensorMap mA = tmA, mB = tmB, mY = tmY;
   GemmArgs args = a;
   int m2 = num_m2, nn = num_n, gm = c.group_m;
-  void* params[] = {&mA, &mB, &args, &m2, &nn, &gm};
+  void* params[] = {&mA, &mB, &mY, &args, &m2, &nn, &gm};
   return cudaLaunchKernelExC(&cfg, e->fn, params);
 }
 

@@ -47,8 +47,8 @@ int tc2_threads();
 int tc2_max_stages(int bn, int smem_optin);
 cudaError_t tc2_prepare(int bn, int stages);
 cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out);
-cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                       const TcConfig& c, cudaStream_t s);
+cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                       const GemmArgs& a, const TcConfig& c, cudaStream_t s);
 
 // ---- split-K decode kernel (small M, swap-AB, cluster reduce) -------------
 struct DecConfig {
