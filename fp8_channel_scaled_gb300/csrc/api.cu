@@ -54,6 +54,11 @@ struct DevState {
   cudaMemPool_t pool = nullptr;  // private stream-ordered pool for repitch workspaces,
   bool pool_failed = false;      // created on first pooled use, never by the no-alloc entry
   void* noalloc_ws = nullptr;    // device address of g_noalloc_workspace on this device
+  // Occupancy of each kernel configuration, queried once on first use so that
+  // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
+  int tc2_pairs[5][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
+  int dec_blocks[3][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
+  int dec_clusters[3][6][2][9];  // ... [splits]: resident clusters
 };
 
 std::mutex g_mu;
@@ -94,6 +99,9 @@ int device_state(int dev, DevState** out) {
   *out = &d;
   if (d.init) return d.status;
   d.init = true;
+  std::memset(d.tc2_pairs, 0xff, sizeof(d.tc2_pairs));
+  std::memset(d.dec_blocks, 0xff, sizeof(d.dec_blocks));
+  std::memset(d.dec_clusters, 0xff, sizeof(d.dec_clusters));
   d.status = FP8GEMM_EDEVICE;
   int major = 0, minor = 0;
   if (cudaSetDevice(dev) != cudaSuccess ||
@@ -168,6 +176,72 @@ cudaMemPool_t workspace_pool(DevState& d, int dev) {
   return d.pool;
 }
 
+template <typename T, size_t n>
+int index_of(const T (&arr)[n], T v) {
+  for (size_t i = 0; i < n; ++i)
+    if (arr[i] == v) return static_cast<int>(i);
+  return -1;
+}
+
+// Resident CTA pairs of the pair kernel (bn, stages) on the whole device.
+int tc2_pairs(DevState& d, int bn, int stages) {
+  const int i = index_of(kTcTiles, bn), j = index_of(kTc2Stages, stages);
+  if (i < 0 || j < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& v = d.tc2_pairs[i][j];
+  if (v < 0) {
+    int pairs = 0;
+    if (tc2_max_active_pairs(bn, stages, d.sm_count & ~1, &pairs) != cudaSuccess) {
+      cudaGetLastError();
+      pairs = 0;
+    }
+    v = std::max(0, std::min(pairs, d.sm_count / 2));
+  }
+  return v;
+}
+
+// Resident decode CTAs per SM, or 0 if the configuration cannot run.  The
+// tensor-memory budget (512 columns per SM) must cover every resident CTA, or
+// a CTA's allocation would wait for another CTA to finish.
+int dec_occupancy(DevState& d, int mp, int stages, bool realign) {
+  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages);
+  if (i < 0 || j < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& v = d.dec_blocks[i][j][realign ? 1 : 0];
+  if (v < 0) {
+    v = 0;
+    const int smem = dec_smem_bytes(mp, stages, realign);
+    int blocks = 0;
+    if (smem >= 0 && smem <= d.smem_optin) {
+      if (dec_blocks_per_sm(mp, stages, realign, &blocks) != cudaSuccess) {
+        cudaGetLastError();
+        blocks = 0;
+      }
+      if (blocks * dec_tmem_cols(mp) <= 512) v = std::max(0, blocks);
+    }
+  }
+  return v;
+}
+
+// Resident clusters of `splits` decode CTAs on the whole device.  Cluster
+// placement (the CTAs of a cluster share a GPC) limits this below the per-SM
+// count.  The query uses a grid large enough not to cap the answer.
+int dec_clusters(DevState& d, int mp, int stages, bool realign, int splits) {
+  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages);
+  if (i < 0 || j < 0 || splits < 1 || splits > 8) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& v = d.dec_clusters[i][j][realign ? 1 : 0][splits];
+  if (v < 0) {
+    int c = 0;
+    if (dec_max_active_clusters(mp, stages, realign, splits, splits * 1024, &c) != cudaSuccess) {
+      cudaGetLastError();
+      c = 0;
+    }
+    v = std::max(0, c);
+  }
+  return v;
+}
+
 // TMA descriptor of a row-major byte matrix [rows, K], box [box_rows, 128],
 // 128-byte swizzle, out-of-bounds elements read as zero.
 int encode_operand(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
@@ -206,21 +280,6 @@ struct Plan {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
 
-// Resident decode CTAs per SM, or 0 if the configuration cannot run.  The
-// tensor-memory budget (512 columns per SM) must cover every resident CTA, or
-// a CTA's allocation would wait for another CTA to finish.
-int dec_occupancy(const DevState& d, int mp, int stages, bool realign) {
-  const int smem = dec_smem_bytes(mp, stages, realign);
-  if (smem < 0 || smem > d.smem_optin) return 0;
-  int blocks = 0;
-  if (dec_blocks_per_sm(mp, stages, realign, &blocks) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  if (blocks * dec_tmem_cols(mp) > 512) return 0;
-  return blocks;
-}
-
 // Main path tile choice.  For each N tile (with the deepest ring that fits)
 // and each tile kind -- one-CTA 128-row tiles or CTA-pair 256-row tiles --
 // estimate waves x tile width, i.e. the wave quantisation of the persistent
@@ -228,7 +287,7 @@ int dec_occupancy(const DevState& d, int mp, int stages, bool realign) {
 // tile).  One-CTA tiles pay for the larger share of B each SM stages and
 // reads (measured about 1.3x slower per tile); narrower tiles pay for their
 // lower operand reuse.  The realigning producer exists for one-CTA tiles only.
-int choose_tc(const DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
+int choose_tc(DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
               TcConfig* out) {
   double best = 1e300;
   TcConfig pick{};
@@ -244,12 +303,7 @@ int choose_tc(const DevState& d, int M, int N, bool realign, const fp8gemm_optio
             tc2_smem_bytes(bn, stages) > d.smem_optin)
           continue;
         const long long tiles = static_cast<long long>((M + 255) / 256) * ((N + bn - 1) / bn);
-        int pairs = 0;
-        if (tc2_max_active_pairs(bn, stages, d.sm_count & ~1, &pairs) != cudaSuccess) {
-          cudaGetLastError();
-          continue;
-        }
-        pairs = std::min(pairs, d.sm_count / 2);
+        const int pairs = tc2_pairs(d, bn, stages);
         if (pairs <= 0) continue;
         units = static_cast<int>(std::min<long long>(tiles, pairs));
         const long long waves = (tiles + pairs - 1) / pairs;
@@ -280,7 +334,7 @@ int choose_tc(const DevState& d, int M, int N, bool realign, const fp8gemm_optio
   return FP8GEMM_OK;
 }
 
-int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int K,
+int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
               const fp8gemm_options* opt, Plan* pl) {
   fp8gemm_options o;
   std::memset(&o, 0, sizeof(o));
@@ -345,12 +399,7 @@ int make_plan(const DevState& d, const void* x, const void* w, int M, int N, int
     const int s_max = std::max(1, std::min(8, num_kb));
     for (int s = 1; s <= s_max; ++s) {
       if (o.splits && s != o.splits) continue;
-      int clusters = 0;
-      if (dec_max_active_clusters(mp, stages, realign, s, n_tiles * s, &clusters) !=
-          cudaSuccess) {
-        cudaGetLastError();
-        continue;
-      }
+      const int clusters = dec_clusters(d, mp, stages, realign, s);
       if (clusters <= 0) continue;
       const long long waves = (n_tiles + clusters - 1) / clusters;
       const int per_cta = (num_kb + s - 1) / s;

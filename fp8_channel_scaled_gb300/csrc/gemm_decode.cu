@@ -107,6 +107,11 @@ __global__ void __launch_bounds__(kThreads)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Global memory (operands, scales, y) is touched only after the preceding
+  // grids of the stream have completed; the set-up above overlaps their tail.
+  // Tensor memory is allocated only after the wait, so this CTA never holds
+  // it while it waits for another grid.
+  griddep_wait();
   if (warp == kMmaWarp) {
     tmem_alloc(holder_addr, C::kTmemCols);
     tmem_relinquish();
@@ -119,6 +124,10 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *holder;
+  // Our dependents may launch once every CTA of this grid holds its tensor
+  // memory: a dependent CTA sharing an SM can then only wait for ours to
+  // free it, never take it first.
+  griddep_launch_dependents();
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
 
   if (warp < 4) {
@@ -380,13 +389,14 @@ cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(c.splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  set_pdl(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   CUtensorMap mA = tmA, mB = tmB;
   GemmArgs args = a;
   int splits = c.splits;

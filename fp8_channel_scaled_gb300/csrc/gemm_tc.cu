@@ -100,6 +100,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Global memory (operands, scales, y) is touched only after the preceding
+  // grids of the stream have completed; the set-up above overlaps their tail.
+  // Tensor memory is allocated only after the wait, so this CTA never holds
+  // it while it waits for another grid.
+  griddep_wait();
   if (warp == kMmaWarp) {
     tmem_alloc(holder_addr, C::kTmemCols);
     tmem_relinquish();
@@ -110,6 +115,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *holder;
+  // Our dependents may launch once every CTA of this grid holds its tensor
+  // memory: a dependent CTA sharing an SM can then only wait for ours to
+  // free it, never take it first.
+  griddep_launch_dependents();
 
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
   const int num_tiles = num_m_blk * num_n_blk;
@@ -358,8 +367,16 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
   int gm = c.group_m;
   void* params[] = {&mA, &mB, &args, const_cast<int*>(&num_m_blk), const_cast<int*>(&num_n_blk),
                     &gm};
-  return cudaLaunchKernel(e->fn, dim3(c.grid), dim3(e->threads), params,
-                          static_cast<size_t>(e->smem), s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(e->threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  set_pdl(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, e->fn, params);
 }
 
 }  // namespace fp8g

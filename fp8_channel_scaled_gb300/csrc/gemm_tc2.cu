@@ -105,6 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Global memory (operands, scales, y) is touched only after the preceding
+  // grids of the stream have completed; the set-up above overlaps their tail.
+  // Tensor memory is allocated only after the wait, so this CTA never holds
+  // it while it waits for another grid.
+  griddep_wait();
   if (warp == kMmaWarp) {
     tmem_alloc_pair(holder_addr, C::kTmemCols);
     tmem_relinquish_pair();
@@ -118,6 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *holder;
+  // Our dependents may launch once every CTA of this grid holds its tensor
+  // memory: a dependent CTA sharing an SM can then only wait for ours to
+  // free it, never take it first.
+  griddep_launch_dependents();
 
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
   const int num_tiles = num_m2_blk * num_n_blk;
@@ -217,23 +226,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool zero_acc = (num_kb == 0);
     const bool tma_y = p.vec_store != 0;
     const uint32_t stg = sbase + static_cast<uint32_t>(C::kStgOff) + warp * 2u * kStgBytes;
+    constexpr int kChunks = BN / 32;
     for (int t = pair; t < num_tiles; t += num_pairs) {
       int mb, nb;
       tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
+      // this lane's scale of every chunk, fetched before the accumulator is ready
+      float scv[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int col = nb * BN + c * 32 + static_cast<int>(lane);
+        scv[c] = col < p.N ? __ldg(p.scale + col) : 0.f;
+      }
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
       tc_fence_after_sync();
       const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
       const int row = row0 + static_cast<int>(lane);
       const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
       uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c, ++chunk_no) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, v);
+      // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
+      // is scaled, rounded and stored (its registers are read only after the
+      // next tcgen05.wait::ld)
+      uint32_t va[32], vb[32];
+      tmem_ld_32x32b_x32(t_row, va);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c, ++chunk_no) {
         tmem_ld_wait();
+        if (c + 1 < kChunks) {
+          if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
+          else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+        }
+        const uint32_t* v = (c & 1) ? vb : va;
         const int col0 = nb * BN + c * 32;
-        const float sc =
-            (col0 + static_cast<int>(lane) < p.N) ? __ldg(p.scale + col0 + lane) : 0.f;
+        const float sc = scv[c];
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -280,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    // every store must have finished reading shared memory (and be issued to
-    // global memory) before the CTA exits
-    if (tma_y && lane == 0) tma_store_wait_all<0>();
+    // every store must have finished reading shared memory before the CTA
+    // exits (the writes themselves complete with the grid)
+    if (tma_y && lane == 0) tma_store_wait_read<0>();
     __syncwarp();
   }
 
@@ -371,13 +395,14 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  set_pdl(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   CUtensorMap mA = tmA, mB = tmB, mY = tmY;
   GemmArgs args = a;
   int m2 = num_m2, nn = num_n, gm = c.group_m;

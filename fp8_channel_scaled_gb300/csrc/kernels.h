@@ -51,6 +51,15 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
                        const GemmArgs& a, const TcConfig& c, cudaStream_t s);
 
 // ---- split-K decode kernel (small M, swap-AB, cluster reduce) -------------
+// Programmatic dependent launch: the kernel may be launched, and run its
+// prologue, while the previous kernel of the stream is still finishing.  Each
+// kernel of this library waits in griddep_wait() before it touches global
+// memory, so stream order still holds for every byte it reads or writes.
+inline void set_pdl(cudaLaunchAttribute& attr) {
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+}
+
 struct DecConfig {
   int mp;          // M padded to the MMA N dimension (32, 64 or 128)
   int stages;      // shared-memory pipeline depth

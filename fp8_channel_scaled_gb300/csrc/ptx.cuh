@@ -126,6 +126,23 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, un
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch
+// ----------------------------------------------------------------------------
+// Let the next kernel of the stream (launched with programmatic stream
+// serialization) start its launch and prologue now; it still waits in
+// griddep_wait() until this grid has completed.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this kernel depends on have completed and their
+// memory operations are visible.  A no-op when launched without programmatic
+// stream serialization.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // proxy fences
 // ----------------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async

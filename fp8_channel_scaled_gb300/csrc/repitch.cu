@@ -30,6 +30,8 @@ constexpr int kRowsPerBlock = 8;
 // matrix (M + N rows); its threads walk the rows' 16-byte output chunks with
 // block-local 32-bit indices, kIlp chunks in flight per thread.
 __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int cpr = a.Kp / 16;  // chunks per row
   const long long row0 = static_cast<long long>(blockIdx.x) * kRowsPerBlock;
   const long long rows_total = a.rows_x + a.rows_w;
@@ -81,8 +83,15 @@ cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   if (rows <= 0 || a.Kp <= 0) return cudaSuccess;
   const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  repitch_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  set_pdl(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, repitch_kernel, a);
 }
 
 }  // namespace fp8g
