@@ -26,12 +26,13 @@ class _COptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("force_realign", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("splits", ctypes.c_int),
                 ("no_workspace", ctypes.c_int), ("mma_ctas", ctypes.c_int),
-                ("reserved", ctypes.c_int),
+                ("split_tail", ctypes.c_int), ("reserved", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
-                    "threads", "smem_bytes", "launches", "repitch", "occupancy")
+                    "threads", "smem_bytes", "launches", "repitch", "occupancy", "split_tiles",
+                    "tail_workers")
 
 
 class _CPlan(ctypes.Structure):
@@ -48,6 +49,7 @@ class Options:
     splits: int = 0
     no_workspace: bool = False
     mma_ctas: int = 0           # main path: 0 auto, 1 one-CTA tiles, 2 CTA-pair tiles
+    split_tail: bool = False    # share the last partial wave's tiles out by K (needs a workspace)
     workspace: int = 0          # device pointer (e.g. tensor.data_ptr()), 0 = library pool
     workspace_bytes: int = 0
 
@@ -57,6 +59,7 @@ class Options:
         o.tile_n, o.stages, o.splits = int(self.tile_n), int(self.stages), int(self.splits)
         o.no_workspace = int(bool(self.no_workspace))
         o.mma_ctas = int(self.mma_ctas)
+        o.split_tail = int(bool(self.split_tail))
         o.workspace = int(self.workspace) or None
         o.workspace_bytes = int(self.workspace_bytes)
         return o
@@ -77,6 +80,8 @@ class Plan:
     launches: int
     repitch: int
     occupancy: int
+    split_tiles: int
+    tail_workers: int
     workspace_bytes: int
 
 

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -59,6 +60,7 @@ struct DevState {
   int tc2_pairs[5][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
   int dec_blocks[3][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
   int dec_clusters[3][6][2][9];  // ... [splits]: resident clusters
+  std::atomic<unsigned long long> calls{0};  // split-tail calls launched (epoch source)
 };
 
 std::mutex g_mu;
@@ -86,7 +88,7 @@ unsigned long long budget_ns() {
 
 const int kTcTiles[] = {256, 224, 192, 160, 128};
 const int kTcStages[] = {3, 4, 5, 6, 7};
-const int kTc2Stages[] = {6, 8};
+const int kTc2Stages[] = {3, 4};
 const int kDecMp[] = {32, 64, 128};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
@@ -273,9 +275,27 @@ struct Plan {
   fp8gemm_plan pub;
   TcConfig tc;
   DecConfig dec;
-  int Kp;               // row pitch of the repitched operands
-  size_t x_off, w_off;  // offsets of the repitched x and w inside the workspace
+  int Kp;                     // row pitch of the repitched operands
+  size_t x_off, w_off;        // offsets of the repitched x and w inside the workspace
+  size_t part_off, flag_off;  // offsets of the split-tail partial sums and flags
 };
+
+// Most segments a split tile is cut into.  Its owner adds the other
+// segments' partial sums (256 x BN x 4 bytes each) before it can write y; the
+// pair kernel stages one of them in shared memory, so two segments keep the
+// fix-up to one bulk copy.
+constexpr int kMaxSegmentsPerTile = 2;
+
+// CTA pairs that share the split tail of `tiles` tiles on `pairs` pairs, or
+// 0 when splitting does not shorten the last wave.
+int tail_workers_for(long long tiles, int pairs, int num_kb) {
+  if (pairs <= 0 || num_kb <= 0) return 0;
+  const long long rem = tiles % pairs;
+  if (rem == 0) return 0;
+  long long tw = std::min<long long>(pairs, rem * kMaxSegmentsPerTile);
+  tw = std::min<long long>(tw, rem * num_kb);  // every range at least one K block
+  return tw > rem ? static_cast<int>(tw) : 0;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
@@ -287,8 +307,8 @@ size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
 // tile).  One-CTA tiles pay for the larger share of B each SM stages and
 // reads (measured about 1.3x slower per tile); narrower tiles pay for their
 // lower operand reuse.  The realigning producer exists for one-CTA tiles only.
-int choose_tc(DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
-              TcConfig* out) {
+int choose_tc(DevState& d, int M, int N, int num_kb, bool realign, bool can_split,
+              const fp8gemm_options& o, TcConfig* out) {
   double best = 1e300;
   TcConfig pick{};
   for (int ctas : {2, 1}) {
@@ -305,12 +325,23 @@ int choose_tc(DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
         const long long tiles = static_cast<long long>((M + 255) / 256) * ((N + bn - 1) / bn);
         const int pairs = tc2_pairs(d, bn, stages);
         if (pairs <= 0) continue;
-        units = static_cast<int>(std::min<long long>(tiles, pairs));
-        const long long waves = (tiles + pairs - 1) / pairs;
-        const double cost = static_cast<double>(waves) * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
+        // with a split tail the last wave costs its share of the tail's K
+        // blocks plus the owners' reads of the other segments' partial sums
+        const int tw = can_split ? tail_workers_for(tiles, pairs, num_kb) : 0;
+        double waves;
+        if (tw > 0) {
+          const long long rem = tiles % pairs;
+          waves = static_cast<double>(tiles / pairs) + static_cast<double>(rem) / tw +
+                  0.05 * static_cast<double>(tw) / static_cast<double>(rem);
+          units = pairs;
+        } else {
+          waves = static_cast<double>((tiles + pairs - 1) / pairs);
+          units = static_cast<int>(std::min<long long>(tiles, pairs));
+        }
+        const double cost = waves * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
         if (cost < best - 1e-9) {
           best = cost;
-          pick = TcConfig{2, bn, stages, false, 2 * units, 16};
+          pick = TcConfig{2, bn, stages, false, 2 * units, 16, tw};
         }
       } else {
         stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
@@ -324,7 +355,7 @@ int choose_tc(DevState& d, int M, int N, bool realign, const fp8gemm_options& o,
             1.3 * static_cast<double>(waves) * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
         if (cost < best - 1e-9) {
           best = cost;
-          pick = TcConfig{1, bn, stages, realign, units, 16};
+          pick = TcConfig{1, bn, stages, realign, units, 16, 0};
         }
       }
     }
@@ -348,8 +379,8 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
   // Main path with rows TMA cannot tile: repitch into a workspace first,
   // unless the caller forbids it or asks for the in-kernel loader.
-  const bool repitch = path == FP8GEMM_PATH_MAIN && K > 0 && !tma_ok && !o.force_realign &&
-                       !o.no_workspace && (o.workspace || !d.pool_failed);
+  const bool can_ws = !o.no_workspace && (o.workspace || !d.pool_failed);
+  const bool repitch = path == FP8GEMM_PATH_MAIN && K > 0 && !tma_ok && !o.force_realign && can_ws;
   // K == 0 has nothing to load; the realigning variant then issues no copy
   // and needs no tensor map.
   const bool realign = !repitch && (o.force_realign != 0 || !tma_ok || K == 0);
@@ -365,9 +396,20 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   }
 
   if (path == FP8GEMM_PATH_MAIN) {
-    int st = choose_tc(d, M, N, realign, o, &pl->tc);
+    const int num_kb = (K + 127) / 128;
+    int st = choose_tc(d, M, N, num_kb, realign, can_ws && o.split_tail && K > 0, o, &pl->tc);
     if (st != FP8GEMM_OK) return st;
     const bool pair = pl->tc.ctas == 2;
+    if (pl->tc.tail_workers > 0) {
+      // partial sums and flags of the split tail, after the repitch copies
+      const size_t slots = static_cast<size_t>(pl->tc.tail_workers);
+      pl->part_off = align256(pl->pub.workspace_bytes);
+      pl->flag_off = pl->part_off + align256(slots * 2u * 128u * pl->tc.bn * sizeof(float));
+      pl->pub.workspace_bytes = pl->flag_off + align256(slots * 8u * sizeof(unsigned long long));
+      const long long tiles = static_cast<long long>((M + 255) / 256) * ((N + pl->tc.bn - 1) / pl->tc.bn);
+      pl->pub.split_tiles = static_cast<int>(tiles % (pl->tc.grid / 2));
+      pl->pub.tail_workers = pl->tc.tail_workers;
+    }
     pl->pub.tile_m = pair ? 256 : 128;
     pl->pub.tile_n = pl->tc.bn;
     pl->pub.stages = pl->tc.stages;
@@ -451,8 +493,8 @@ int pointer_device(const void* p) {
 
 // Enqueue the planned GEMM kernel.  xa / wa are the operands it reads (the
 // caller's, or their repitched copies) with row pitch Ka.
-int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* wa, int Ka,
-                const float* scale, void* y, int M, int N, cudaStream_t s) {
+int launch_gemm(const Plan& pl, DevState& d, const void* xa, const void* wa, int Ka,
+                const float* scale, void* y, int M, int N, uint8_t* ws, cudaStream_t s) {
   GemmArgs a{};
   a.x = static_cast<const uint8_t*>(xa);
   a.w = static_cast<const uint8_t*>(wa);
@@ -465,6 +507,18 @@ int launch_gemm(const Plan& pl, const DevState& d, const void* xa, const void* w
   a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
   a.err = d.err_word;
   a.budget_ns = budget_ns();
+  if (pl.pub.path == FP8GEMM_PATH_MAIN && pl.tc.tail_workers > 0) {
+    if (!ws) return FP8GEMM_EINVAL;
+    a.tail_workers = pl.tc.tail_workers;
+    a.partials = reinterpret_cast<float*>(ws + pl.part_off);
+    a.flags = reinterpret_cast<unsigned long long*>(ws + pl.flag_off);
+    // a distinct, well-mixed value per call (the splitmix64 finaliser of a
+    // counter), so that neither old flags nor leftover workspace bytes match it
+    unsigned long long z = d.calls.fetch_add(1) + 1;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    a.epoch = z ^ (z >> 31);  // a bijection of z >= 1, hence never 0
+  }
   // TMA descriptors are only meaningful on the TMA path (and need K >= 1);
   // the realigning producer reads x and w through plain pointers.
   CUtensorMap tmA, tmB;
@@ -525,6 +579,28 @@ int noalloc_workspace(DevState& d, uint8_t** out) {
   return FP8GEMM_OK;
 }
 
+// Enqueue a planned call whose workspace `ws` (pl.pub.workspace_bytes) is
+// in hand: the repitch copies first, if any, then the GEMM on the operands it
+// reads.
+int run_with_workspace(const Plan& pl, DevState& d, const void* x, const void* w, int K,
+                       const float* scale, void* y, int M, int N, uint8_t* ws, cudaStream_t s) {
+  if (!pl.pub.repitch) return launch_gemm(pl, d, x, w, K, scale, y, M, N, ws, s);
+  RepitchArgs r{};
+  r.x = static_cast<const uint8_t*>(x);
+  r.w = static_cast<const uint8_t*>(w);
+  r.xo = ws + pl.x_off;
+  r.wo = ws + pl.w_off;
+  r.K = K;
+  r.Kp = pl.Kp;
+  r.rows_x = M;
+  r.rows_w = N;
+  if (launch_repitch(r, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  return launch_gemm(pl, d, r.xo, r.wo, pl.Kp, scale, y, M, N, ws, s);
+}
+
 }  // namespace
 }  // namespace fp8g
 
@@ -559,10 +635,11 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   st = make_plan(*d, x, w, M, N, K, opt, &pl);
   if (st != FP8GEMM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!pl.pub.repitch) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
-
-  // repitch x and w into the workspace, then run the TMA kernel on the copies
   const size_t need = pl.pub.workspace_bytes;
+  if (need == 0) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, nullptr, s);
+
+  // workspace (repitch copies and/or split-tail partial sums): the caller's,
+  // or stream-ordered from the device's pool
   uint8_t* ws = nullptr;
   bool pooled = false;
   if (opt && opt->workspace) {
@@ -575,7 +652,8 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
     void* p = nullptr;
     cudaMemPool_t pool = workspace_pool(*d, dev);
     if (!pool || cudaMallocFromPoolAsync(&p, need, pool, s) != cudaSuccess) {
-      // no memory for a workspace: load the unaligned rows in the kernel instead
+      // no memory for a workspace: load unaligned rows in the kernel (and
+      // run the last wave unsplit) instead
       cudaGetLastError();
       fp8gemm_options o2;
       std::memset(&o2, 0, sizeof(o2));
@@ -585,26 +663,12 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
       o2.workspace_bytes = 0;
       st = make_plan(*d, x, w, M, N, K, &o2, &pl);
       if (st != FP8GEMM_OK) return st;
-      return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
+      return launch_gemm(pl, *d, x, w, K, scale, y, M, N, nullptr, s);
     }
     ws = static_cast<uint8_t*>(p);
     pooled = true;
   }
-  RepitchArgs r{};
-  r.x = static_cast<const uint8_t*>(x);
-  r.w = static_cast<const uint8_t*>(w);
-  r.xo = ws + pl.x_off;
-  r.wo = ws + pl.w_off;
-  r.K = K;
-  r.Kp = pl.Kp;
-  r.rows_x = M;
-  r.rows_w = N;
-  if (launch_repitch(r, s) != cudaSuccess) {
-    cudaGetLastError();
-    st = FP8GEMM_ELAUNCH;
-  } else {
-    st = launch_gemm(pl, *d, r.xo, r.wo, pl.Kp, scale, y, M, N, s);
-  }
+  st = run_with_workspace(pl, *d, x, w, K, scale, y, M, N, ws, s);
   if (pooled && cudaFreeAsync(ws, s) != cudaSuccess) {
     cudaGetLastError();
     if (st == FP8GEMM_OK) st = FP8GEMM_ELAUNCH;
@@ -650,23 +714,9 @@ extern "C" int fp8_gemm_scaled_noalloc(const void* x, const void* w, const float
   Plan pl;
   st = make_plan(*d, x, w, M, N, K, &o, &pl);
   if (st != FP8GEMM_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!pl.pub.repitch) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, s);
   if (pl.pub.workspace_bytes > FP8GEMM_NOALLOC_WORKSPACE_BYTES) return FP8GEMM_ESIZE;
-  RepitchArgs r{};
-  r.x = static_cast<const uint8_t*>(x);
-  r.w = static_cast<const uint8_t*>(w);
-  r.xo = ws + pl.x_off;
-  r.wo = ws + pl.w_off;
-  r.K = K;
-  r.Kp = pl.Kp;
-  r.rows_x = M;
-  r.rows_w = N;
-  if (launch_repitch(r, s) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
-  }
-  return launch_gemm(pl, *d, r.xo, r.wo, pl.Kp, scale, y, M, N, s);
+  return run_with_workspace(pl, *d, x, w, K, scale, y, M, N, ws,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,

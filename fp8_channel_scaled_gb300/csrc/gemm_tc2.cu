@@ -15,12 +15,18 @@
 // Roles per CTA: warps 0-3 epilogue (TMEM -> * scale -> bf16 -> swizzled
 // shared-memory staging -> TMA store), warp 4 TMEM allocation (both CTAs)
 // and MMA issue (even CTA, one thread), warps 5-8 TMA producers, one thread
-// each: x of even stages, x of odd stages, w of even stages, w of odd stages
-// (a TMA copy keeps its issuing thread busy for hundreds of cycles, so one
-// thread per operand cannot keep the tensor cores fed).  Synchronisation:
-//   full[s]   in CTA 0 only: CTA 0's x and w producers of stage s arm it, each
-//             with its operand's bytes for both CTAs; both CTAs' loads
-//             complete on it;
+// each: x of a stage's first K block, x of its second, w of its first, w of
+// its second (a TMA copy keeps its issuing thread busy for about a hundred
+// cycles, so one thread per operand cannot keep the tensor cores fed).
+//
+// A stage holds two 128-byte K blocks.  The issuing thread spends about 95
+// cycles per tcgen05.mma and about 70 per barrier wait even when the stage
+// is ready, so with one K block (4 MMAs, 512 tensor cycles at N = 256) per
+// wait and commit, issue rather than the tensor core set the pace; with two
+// (8 MMAs, 1024 cycles) per wait and commit it keeps ahead.
+// Synchronisation:
+//   full[s]   in CTA 0 only: CTA 0's four producers arm it, each with its
+//             box's bytes for both CTAs; both CTAs' loads complete on it;
 //   empty[s]  in both CTAs: the MMA commit multicasts to both;
 //   tfull[a]  in both CTAs: multicast commit after a tile's last K block;
 //   tempty[a] in CTA 0 only: all 8 epilogue warps of the pair arrive on it.
@@ -35,28 +41,35 @@ namespace fp8g {
 namespace {
 
 constexpr int kBK = 128;
-constexpr int kMmaK = 32;
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;   // warps 5-8: (x, even), (x, odd), (w, even), (w, odd) stages
+constexpr int kProdWarp0 = 5;   // warps 5-8: x first half, x second half, w first, w second
+constexpr int kKbPerStage = 2;  // 128-byte K blocks per pipeline stage
 constexpr int kThreads = 288;
 constexpr int kStgBytes = 2048;  // one 32 x 32 bf16 staging box (64-byte swizzle)
 
 template <int BN, int STAGES>
 struct Cfg2 {
-  static constexpr int kABytes = 128 * kBK;        // this CTA's 128 rows of x
+  static constexpr int kABytes1 = 128 * kBK;       // this CTA's 128 rows of x, one K block
   static constexpr int kBRows = BN / 2;            // this CTA's rows of w
-  static constexpr int kBBytes = kBRows * kBK;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBBytes1 = kBRows * kBK;    // ... one K block
+  static constexpr int kABytes = kKbPerStage * kABytes1;
+  static constexpr int kBBytes = kKbPerStage * kBBytes1;
+  static constexpr int kStageBytes = kABytes + kBBytes;  // [x kb0][x kb1][w kb0][w kb1]
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
   static constexpr int kStgOff = STAGES * kStageBytes;            // 4 warps x 2 staging boxes
   static constexpr int kBarOff = kStgOff + kEpiWarps * 2 * kStgBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kNumBars = 2 * STAGES + 5 + kEpiWarps;  // + one per epilogue warp
+  static constexpr int kPartBytes = BN * 128;  // one warp's share of a partial sum (32 x BN fp32)
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(kBRows % 8 == 0, "B half must be whole 8-row swizzle atoms");
-  static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
-  static_assert(STAGES % 2 == 0, "each stage is owned by one x and one w producer");
+  static_assert(kKbPerStage == 1 || kKbPerStage == 2, "K blocks per stage");
+  static_assert(kKbPerStage == 2 || STAGES % 2 == 0, "one-K-block stages alternate producers");
+  static_assert(kABytes1 % 1024 == 0 && kBBytes1 % 1024 == 0,
+                "every K block of a stage must start on a 1024-byte swizzle atom");
+  static_assert(kEpiWarps * kPartBytes <= STAGES * kStageBytes,
+                "a partial sum must fit in the ring it reuses");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -78,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto part_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + w); };
   const uint32_t holder_addr = bar0 + 8u * C::kNumBars;
   volatile uint32_t* holder =
       reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOff + 8 * C::kNumBars);
@@ -94,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 2u);  // the two producers of CTA 0
+      mbar_init(full_bar(s), kKbPerStage == 2 ? 4u : 2u);  // CTA 0's producers of stage s
       mbar_init(empty_bar(s), 1u);
     }
     for (int a = 0; a < 2; ++a) {
@@ -102,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), static_cast<uint32_t>(2 * kEpiWarps));
     }
     mbar_init(mma_done_bar, 1u);
+    for (uint32_t w = 0; w < kEpiWarps; ++w) mbar_init(part_bar(w), 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -131,44 +146,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
   const int num_tiles = num_m2_blk * num_n_blk;
   const int num_kb = p.num_kb;
+  const int tail_workers = p.tail_workers;
 
   if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
       const uint32_t q = warp - kProdWarp0;
       const bool is_a = q < 2;
-      const uint32_t parity = q & 1u;  // stages s with s % 2 == parity
+      // two K blocks per stage: this thread loads K block `sub` of every
+      // stage; one: it loads every other stage (those with it % 2 == sub)
+      const int sub = static_cast<int>(q & 1u);
+      const int half = kKbPerStage == 2 ? sub : 0;
       const CUtensorMap* map = is_a ? &tmA : &tmB;
-      const uint32_t bytes = is_a ? C::kABytes : C::kBBytes;
-      const uint32_t off = is_a ? 0u : static_cast<uint32_t>(C::kABytes);
-      uint32_t it = 0;  // (tile, K block) iteration, shared numbering of all producers
+      const uint32_t bytes = is_a ? C::kABytes1 : C::kBBytes1;
+      const uint32_t off = is_a ? static_cast<uint32_t>(half * C::kABytes1)
+                                : static_cast<uint32_t>(C::kABytes + half * C::kBBytes1);
+      uint32_t it = 0;  // (unit, stage) iteration, shared numbering of all producers
       bool ok = true;
-      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+      WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
+      WorkUnit wu;
+      while (ok && wi.next(wu)) {
         int mb, nb;
-        tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
+        tile_coords(wu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
         const int row = is_a ? mb * 256 + static_cast<int>(rank) * 128
                              : nb * BN + static_cast<int>(rank) * C::kBRows;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          if ((it & 1u) != parity) continue;
+        for (int kb = wu.k0; kb < wu.k1; kb += kKbPerStage, ++it) {
+          if (kKbPerStage == 1 && static_cast<int>(it & 1u) != sub) continue;
           const uint32_t stage = it % STAGES;
           const uint32_t use = it / STAGES;
           if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) {
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
-          tma_load_2d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) + off, map,
-                           mapa_shared(full_bar(stage), 0u), kb * kBK, row);
+          if (kb + half < wu.k1) {
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+            tma_load_2d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) + off, map,
+                             mapa_shared(full_bar(stage), 0u), (kb + half) * kBK, row);
+          } else if (rank == 0) {
+            mbar_arrive(full_bar(stage));  // odd K-block count: this half stays empty
+          }
         }
       }
-      // Teardown: every load this thread issued (iterations < it of its
-      // parity) must have landed.  CTA 0 sees its full barriers complete;
-      // CTA 1's loads complete on CTA 0's barrier, so it waits for the MMA's
-      // release of the stage instead.  Each stage barrier completes exactly
-      // one phase per use, so the last use's parity is unambiguous.
+      // Teardown: every load this thread issued must have landed.  CTA 0
+      // sees its full barriers complete; CTA 1's loads complete on CTA 0's
+      // barrier, so it waits for the MMA's release of the stage instead.
+      // Each stage barrier completes exactly one phase per use, so the last
+      // use's parity is unambiguous.
       for (uint32_t back = 1; back <= STAGES && back <= it; ++back) {
         const uint32_t i = it - back;
-        if ((i & 1u) != parity) continue;
+        if (kKbPerStage == 1 && static_cast<int>(i & 1u) != sub) continue;
         const uint32_t ph = (i / STAGES) & 1u;
         if (rank == 0)
           drain_wait(full_bar(i % STAGES), ph, p.err, p.budget_ns);
@@ -181,30 +207,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (CTA 0)
     if (rank == 0 && lane == 0) {
       constexpr uint32_t kIdesc = idesc_e4m3_f32(256, BN);
+      // descriptors of stage 0; stage s adds s * kStageBytes to the 16-byte
+      // start-address field (shared addresses stay below 2^18, no carry out)
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sA(0));
+      const uint64_t b_desc0 = sdesc_kmajor_sw128(sB(0));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+      bool ready = false;  // full[stage] already seen complete (tested during the last issue)
+      WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
+      WorkUnit wu;
+      while (ok && wi.next(wu)) {
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wc, kErrWaitMma)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, wc, kErrWaitMma)) {
+        for (int kb = wu.k0; kb < wu.k1; kb += kKbPerStage) {
+          if (!ready && !mbar_wait_bounded(full_bar(stage), phase, wc, kErrWaitMma)) {
             ok = false;
             break;
           }
           // the TMA bytes reach the MMA through the full barrier alone: no tcgen05
-          // fence per K block (one would hold the issue back until earlier MMAs drain)
-          const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
-          const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
-#pragma unroll
-          for (int k = 0; k < kBK / kMmaK; ++k)
-            tc_mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, kIdesc,
-                           (kb > 0 || k > 0) ? 1u : 0u);
-          tc_commit_pair_mc(empty_bar(stage), 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          // fence per stage (one would hold the issue back until earlier MMAs drain)
+          const uint32_t next = stage + 1 == STAGES ? 0u : stage + 1;
+          const uint32_t next_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
+          ready = tc_mma_stage_pair(d_tmem, a_desc0 + stage * (C::kStageBytes >> 4),
+                                    b_desc0 + stage * (C::kStageBytes >> 4), kIdesc,
+                                    kb > wu.k0 ? 1u : 0u,
+                                    (kKbPerStage == 2 && kb + 1 < wu.k1) ? 1u : 0u,
+                                    C::kABytes1 >> 4, C::kBBytes1 >> 4, empty_bar(stage), 0x3,
+                                    full_bar(next), next_phase);
+          stage = next;
+          phase = next_phase;
         }
         if (!ok) break;
         tc_commit_pair_mc(tfull_bar(acc), 0x3);
@@ -222,79 +254,151 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two 64-byte-swizzled staging boxes and let one lane TMA-store it (the
     // store clips rows >= M and columns >= N).  Without a usable y map
     // (N % 8 != 0 or y not 16-byte aligned) rows are stored directly.
-    uint32_t acc = 0, acc_phase = 0, chunk_no = 0;
+    uint32_t acc = 0, acc_phase = 0, chunk_no = 0, part_phase = 0;
     const bool zero_acc = (num_kb == 0);
     const bool tma_y = p.vec_store != 0;
     const uint32_t stg = sbase + static_cast<uint32_t>(C::kStgOff) + warp * 2u * kStgBytes;
     constexpr int kChunks = BN / 32;
-    for (int t = pair; t < num_tiles; t += num_pairs) {
+    // This warp's share of worker q's published partial sum: 32 rows x BN
+    // columns stored [chunk][column][row], so that each store and load
+    // instruction of the warp covers 128 contiguous bytes.
+    constexpr int kPartFloats = kChunks * 32 * 32;
+    const uint32_t slot = rank * 4u + warp;
+    auto part_of = [&](int q) {
+      return p.partials + (static_cast<size_t>(q) * 8u + slot) * kPartFloats;
+    };
+    WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
+    WorkUnit wu;
+    while (wi.next(wu)) {
       int mb, nb;
-      tile_coords(t, num_m2_blk, num_n_blk, group_m, mb, nb);
-      // this lane's scale of every chunk, fetched before the accumulator is ready
-      float scv[kChunks];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int col = nb * BN + c * 32 + static_cast<int>(lane);
-        scv[c] = col < p.N ? __ldg(p.scale + col) : 0.f;
-      }
-      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
-      tc_fence_after_sync();
+      tile_coords(wu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
       const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
       const int row = row0 + static_cast<int>(lane);
       const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
-      uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
       // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
-      // is scaled, rounded and stored (its registers are read only after the
-      // next tcgen05.wait::ld)
+      // is used (its registers are read only after the next tcgen05.wait::ld)
       uint32_t va[32], vb[32];
-      tmem_ld_32x32b_x32(t_row, va);
+      if (!wu.owner) {
+        // ---- a segment that does not hold the tile's first K block: publish
+        // its fp32 partial sum for the owner
+        if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
+        tc_fence_after_sync();
+        float* dst = part_of(pair) + lane;
+        tmem_ld_32x32b_x32(t_row, va);
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c, ++chunk_no) {
-        tmem_ld_wait();
-        if (c + 1 < kChunks) {
-          if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
-          else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
-        }
-        const uint32_t* v = (c & 1) ? vb : va;
-        const int col0 = nb * BN + c * 32;
-        const float sc = scv[c];
-        uint32_t packed[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
-          const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
-          const float a0 = zero_acc ? 0.f : __uint_as_float(v[2 * j]);
-          const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
-          packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
-        }
-        if (tma_y) {
-          const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
-          if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
-            if (lane == 0) tma_store_wait_read<1>();
-            __syncwarp();
+        for (int c = 0; c < kChunks; ++c) {
+          tmem_ld_wait();
+          if (c + 1 < kChunks) {
+            if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
+            else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
           }
-          // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
-          const uint32_t rb = buf + lane * 64u;
+          const uint32_t* v = (c & 1) ? vb : va;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
-                   make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                              packed[4 * q + 3]));
-          fence_proxy_async_smem();
-          __syncwarp();
+          for (int j = 0; j < 32; ++j) __stcg(dst + (c * 32 + j) * 32, __uint_as_float(v[j]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u64(p.flags + static_cast<size_t>(pair) * 8u + slot, p.epoch);
+      } else {
+        // ---- the tile's owner: own accumulator (+ the partial sums of
+        // workers pair+1 .. q_end-1, in that order) * scale -> bf16 -> y.
+        // Each lane's scale of every chunk is fetched before the accumulator
+        // is ready.
+        float scv[kChunks];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          const int col = nb * BN + c * 32 + static_cast<int>(lane);
+          scv[c] = col < p.N ? __ldg(p.scale + col) : 0.f;
+        }
+        if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
+        tc_fence_after_sync();
+        // The partial sum of the first contributor is brought into shared
+        // memory with one bulk copy: a tile with contributors is always its
+        // owner's last unit, so the operand ring is idle (every MMA of the
+        // pair has completed) and holds it.  Any further contributor (the
+        // host cuts tiles into at most two segments) is read from L2.
+        bool have_parts = true;
+        const bool staged = wu.q_end > pair + 1;
+        if (staged) {
           if (lane == 0) {
-            // boxes entirely past M or N are not issued; the (possibly empty)
-            // group is committed either way so that the buffer accounting
-            // above always refers to the same chunk
-            if (row0 < p.M && col0 < p.N) tma_store_2d(&tmY, buf, col0, row0);
-            tma_store_commit();
+            for (int q = pair + 1; q < wu.q_end && have_parts; ++q)
+              have_parts = flag_wait_bounded(p.flags + static_cast<size_t>(q) * 8u + slot,
+                                             p.epoch, p.err, abort_flag, p.budget_ns);
+            if (have_parts) {
+              fence_proxy_async_global();
+              mbar_arrive_expect_tx(part_bar(warp), C::kPartBytes);
+              bulk_load_g2s(sbase + warp * C::kPartBytes, part_of(pair + 1), C::kPartBytes,
+                            part_bar(warp));
+            }
           }
-        } else if (row < p.M) {
+          have_parts = __shfl_sync(0xffffffffu, have_parts ? 1 : 0, 0) != 0;
+          if (have_parts)
+            have_parts = mbar_wait_bounded(part_bar(warp), part_phase, wc, kErrWaitPartial);
+          part_phase ^= 1u;
+        }
+        const int q_end = have_parts ? wu.q_end : pair + 1;
+        const float* staged_part =
+            reinterpret_cast<const float*>(gbase + warp * C::kPartBytes) + lane;
+        uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
+        tmem_ld_32x32b_x32(t_row, va);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col0 + j < p.N)
-              yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
-                                                             : (packed[j >> 1] & 0xFFFFu));
+        for (int c = 0; c < kChunks; ++c, ++chunk_no) {
+          tmem_ld_wait();
+          if (c + 1 < kChunks) {
+            if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
+            else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+          }
+          const uint32_t* v = (c & 1) ? vb : va;
+          float a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = zero_acc ? 0.f : __uint_as_float(v[j]);
+          if (q_end > pair + 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] += staged_part[(c * 32 + j) * 32];
+          }
+          for (int q = pair + 2; q < q_end; ++q) {
+            const float* src = part_of(q) + c * 1024 + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
+          }
+          const int col0 = nb * BN + c * 32;
+          const float sc = scv[c];
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+            const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+            packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+          }
+          if (tma_y) {
+            const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
+            if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
+              if (lane == 0) tma_store_wait_read<1>();
+              __syncwarp();
+            }
+            // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
+            const uint32_t rb = buf + lane * 64u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+                     make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                packed[4 * q + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              // boxes entirely past M or N are not issued; the (possibly empty)
+              // group is committed either way so that the buffer accounting
+              // above always refers to the same chunk
+              if (row0 < p.M && col0 < p.N) tma_store_2d(&tmY, buf, col0, row0);
+              tma_store_commit();
+            }
+          } else if (row < p.M) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < p.N)
+                yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
+                                                               : (packed[j >> 1] & 0xFFFFu));
+            }
           }
         }
       }
@@ -333,8 +437,8 @@ Entry2 make_entry2() {
 }
 
 const Entry2 kEntries2[] = {
-    make_entry2<256, 6>(), make_entry2<224, 6>(), make_entry2<192, 6>(), make_entry2<160, 8>(),
-    make_entry2<128, 8>(),
+    make_entry2<256, 3>(), make_entry2<224, 3>(), make_entry2<192, 3>(), make_entry2<160, 4>(),
+    make_entry2<128, 4>(),
 };
 
 const Entry2* find2(int bn, int stages) {

@@ -20,6 +20,16 @@ struct GemmArgs {
   int vec_store;         // 1: y rows are 16-byte aligned (N % 8 == 0, y aligned)
   unsigned* err;         // device error word
   unsigned long long budget_ns;  // longest single wait before giving up
+  // Split tail of the CTA-pair kernel (tail_workers == 0: no split; see
+  // WorkIter in sched.cuh): slot q < tail_workers of `partials` holds worker
+  // q's published partial sum, [2 CTAs][4 warps][BN / 32 chunks][32 columns]
+  // [32 rows] fp32; flags[q][2][4] is set to `epoch` once the matching
+  // warp's part is written.  Epochs are unique per device and call, so the
+  // flags never need clearing.
+  int tail_workers;
+  float* partials;
+  unsigned long long* flags;
+  unsigned long long epoch;
 };
 
 // ---- persistent tcgen05 kernel (large M) ---------------------------------
@@ -30,6 +40,7 @@ struct TcConfig {
   bool realign;    // operands loaded by the realigning producer instead of TMA
   int grid;        // persistent CTAs
   int group_m;     // M tiles per raster group
+  int tail_workers;  // CTA pairs sharing the split tail (0: no split; pair kernel only)
 };
 bool tc_config_supported(int bn, int stages, bool realign);
 int tc_smem_bytes(int bn, int stages, bool realign);

@@ -21,6 +21,7 @@ enum : unsigned {
   kErrWaitEpilogue = 1u << 2,   // epilogue gave up waiting for an accumulator
   kErrWaitDrain    = 1u << 3,   // teardown gave up waiting for copies / MMAs in flight
   kErrWaitSelfTest = 1u << 4,   // the deliberate wait of the self-test kernel ran out
+  kErrWaitPartial  = 1u << 5,   // a split tile's owner gave up waiting for a partial sum
 };
 
 // ----------------------------------------------------------------------------
@@ -126,6 +127,39 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, un
 }
 
 // ----------------------------------------------------------------------------
+// cross-CTA publication through global memory
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Wait until *flag == want (a value another CTA of the same grid publishes
+// with st_release_u64).  Bounded like the mbarrier waits.
+static __device__ __noinline__ bool flag_wait_bounded(const unsigned long long* flag,
+                                                      unsigned long long want, unsigned* err,
+                                                      volatile int* abort_flag,
+                                                      uint64_t budget_ns) {
+  if (ld_acquire_u64(flag) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(100);
+    if (ld_acquire_u64(flag) == want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > budget_ns) {
+      *abort_flag = 1;
+      atomicOr(err, kErrWaitPartial);
+      return false;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
 // programmatic dependent launch
 // ----------------------------------------------------------------------------
 // Let the next kernel of the stream (launched with programmatic stream
@@ -151,11 +185,29 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy global accesses (e.g. the acquire
+// of a flag) before its later async-proxy global accesses (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------
 // TMA
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar` as
+// transaction bytes.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // 2-D tiled load of one box into shared memory; completion is reported to
@@ -341,6 +393,65 @@ __device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc,
       "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// One pipeline stage of the CTA-pair MMA issuer in a single asm block:
+//   - test (without blocking) whether the next stage's full barrier
+//     `next_full` has completed phase `next_parity`;
+//   - issue 4 MMAs (K = 32 each) over the stage's first 128-byte K block
+//     (accumulating if `accumulate`, else overwriting D for the first one),
+//     and 4 more over its second K block if `two_kb`;
+//   - commit the stage to the mbarrier `empty` in the CTAs of `cta_mask`;
+//   - return the test's result.
+// The barrier test is issued first and its result read last, so its latency
+// overlaps the MMA issue instead of adding to it.  a_step / b_step: offset
+// of the second K block in descriptor units (bytes / 16).
+__device__ __forceinline__ bool tc_mma_stage_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate, uint32_t two_kb,
+                                                  uint64_t a_step, uint64_t b_step,
+                                                  uint32_t empty, uint16_t cta_mask,
+                                                  uint32_t next_full, uint32_t next_parity) {
+  uint32_t ready;
+  asm volatile(
+      "{\n\t"
+      ".reg .pred pr, pa, ph, pt;\n\t"
+      ".reg .b64 a1, b1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pr, [%10], %11;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "setp.ne.b32 ph, %6, 0;\n\t"
+      "setp.eq.b32 pt, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], %2, %3, %4, pa;\n\t"
+      "add.s64 a1, %2, 2;\n\t"
+      "add.s64 b1, %3, 2;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, %2, 4;\n\t"
+      "add.s64 b1, %3, 4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, %2, 6;\n\t"
+      "add.s64 b1, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, %2, %7;\n\t"
+      "add.s64 b1, %3, %8;\n\t"
+      "@ph tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, a1, 2;\n\t"
+      "add.s64 b1, b1, 2;\n\t"
+      "@ph tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, a1, 2;\n\t"
+      "add.s64 b1, b1, 2;\n\t"
+      "@ph tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "add.s64 a1, a1, 2;\n\t"
+      "add.s64 b1, b1, 2;\n\t"
+      "@ph tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], a1, b1, %4, pt;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%9], %12;\n\t"
+      "selp.b32 %0, 1, 0, pr;\n\t"
+      "}\n"
+      : "=r"(ready)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(two_kb),
+        "l"(a_step), "l"(b_step), "r"(empty), "r"(next_full), "r"(next_parity), "h"(cta_mask)
+      : "memory");
+  return ready != 0;
 }
 
 // Arrive once on the mbarrier at this shared-memory offset in every CTA of

@@ -18,4 +18,83 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   nb = r / gsize;
 }
 
+// Work of one persistent worker (a CTA pair) out of `workers`.
+//
+// Without a split tail, worker r takes tiles r, r + workers, r + 2 workers,
+// ... whole.  With it, only the first floor(tiles / workers) waves are taken
+// whole; the K blocks of the remaining tiles, concatenated in tile order, are
+// divided evenly between the first `tail_workers` workers, each taking one
+// contiguous range, so that the last wave ends after a fraction of a tile
+// instead of some workers running one tile longer than the rest.  A range
+// cut at tile boundaries gives segments.  The segment holding a tile's first
+// K block owns the tile: it adds the partial sums of that tile's other
+// segments and writes y.  Any other segment is the first segment of its
+// worker's range (later segments start on a tile boundary), so each worker
+// publishes at most one partial sum, kept in slot `worker`.  The owner ends
+// its range with its segment of the tile, which the workers after it start
+// theirs with, so it rarely waits.  The host makes every tail range at least
+// one K block long.
+struct WorkUnit {
+  int tile;    // tile index in raster order
+  int k0, k1;  // K blocks [k0, k1) of the tile
+  bool owner;  // true: write y (after adding the partials of workers owner+1 .. q_end-1)
+  int q_end;
+};
+
+struct WorkIter {
+  int me, workers, tail_workers, num_kb, n_full, tail_base, tail_tiles;
+  int u;
+  long long it, te;
+
+  // tail_workers == 0: no split tail.
+  __device__ WorkIter(int me_, int workers_, int num_tiles, int num_kb_, int tail_workers_)
+      : me(me_), workers(workers_), tail_workers(tail_workers_), num_kb(num_kb_), u(0) {
+    if (tail_workers > 0) {
+      n_full = num_tiles / workers;
+      tail_base = n_full * workers;
+      tail_tiles = num_tiles - tail_base;
+    } else {
+      n_full = me < num_tiles ? (num_tiles - 1 - me) / workers + 1 : 0;
+      tail_base = num_tiles;
+      tail_tiles = 0;
+    }
+    it = tail_begin(me);
+    te = tail_begin(me + 1);
+  }
+
+  // First K block (in the concatenated tail) of worker q's range.
+  __device__ long long tail_begin(int q) const {
+    if (tail_workers <= 0) return 0;
+    if (q >= tail_workers) return static_cast<long long>(tail_tiles) * num_kb;
+    return static_cast<long long>(tail_tiles) * num_kb * q / tail_workers;
+  }
+
+  __device__ bool next(WorkUnit& w) {
+    if (u < n_full) {
+      w.tile = me + u * workers;
+      w.k0 = 0;
+      w.k1 = num_kb;
+      w.owner = true;
+      w.q_end = me + 1;
+      ++u;
+      return true;
+    }
+    if (it >= te) return false;
+    const int j = static_cast<int>(it / num_kb);
+    const long long tile_first = static_cast<long long>(j) * num_kb;
+    const long long tile_end = tile_first + num_kb;
+    const long long seg_end = te < tile_end ? te : tile_end;
+    w.tile = tail_base + j;
+    w.k0 = static_cast<int>(it - tile_first);
+    w.k1 = static_cast<int>(seg_end - tile_first);
+    w.owner = (w.k0 == 0);
+    int q = me + 1;
+    if (w.owner)
+      while (q < tail_workers && tail_begin(q) < tile_end) ++q;
+    w.q_end = q;
+    it = seg_end;
+    return true;
+  }
+};
+
 }  // namespace fp8g

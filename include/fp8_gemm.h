@@ -22,8 +22,9 @@
  *   - Ownership: the caller owns every buffer.  The library keeps, per
  *     device, its properties, a 4-byte device error word (see
  *     fp8_gemm_check_device_error) and a private stream-ordered memory pool.
- *     The only device memory a call may take is the repitch workspace of the
- *     main path (see fp8_gemm_workspace_bytes): from the caller when
+ *     The only device memory a call may take is the main path's workspace
+ *     (see fp8_gemm_workspace_bytes): repitched copies of x and w, and the
+ *     split tail's partial sums.  It comes from the caller when
  *     fp8gemm_options.workspace is given, else from that pool with
  *     cudaMallocFromPoolAsync / cudaFreeAsync on the call's stream, so calls
  *     on different streams never share it.
@@ -46,7 +47,7 @@ extern "C" {
  * (identical to cudaStream_t). */
 typedef struct CUstream_st *fp8gemm_stream_t;
 
-#define FP8GEMM_VERSION 1
+#define FP8GEMM_VERSION 2
 
 typedef enum {
     FP8GEMM_OK = 0,
@@ -82,6 +83,11 @@ typedef struct {
                            loaded by the in-kernel realigning producer */
     int mma_ctas;       /* main path: 0 auto, 1 one-CTA 128-row tiles,
                            2 CTA-pair 256-row tiles (tcgen05 cta_group::2) */
+    int split_tail;     /* 1: share the last partial wave's tiles out by K
+                           between CTA pairs (see fp8gemm_plan.split_tiles);
+                           needs a workspace.  Off by default: with this
+                           kernel's epilogue the fix-up costs about what it
+                           saves */
     int reserved;       /* must be zero */
     void *workspace;    /* optional caller workspace (device, 256-byte aligned) */
     size_t workspace_bytes; /* its size; must be >= fp8_gemm_workspace_bytes() */
@@ -103,6 +109,11 @@ typedef struct {
     int launches;       /* kernels launched by one call (0, 1, or 2 with repitch) */
     int repitch;        /* 1: operands are first copied to a 16-byte pitch */
     int occupancy;      /* resident CTAs per SM of the GEMM kernel */
+    int split_tiles;    /* main path, CTA pairs: tiles past the last full wave
+                           whose K blocks are shared out between
+                           tail_workers pairs (0 = no split) */
+    int tail_workers;   /* CTA pairs sharing them; each publishes at most one
+                           fp32 partial sum that the tile's owner adds */
     size_t workspace_bytes; /* device workspace the call needs (0 = none) */
 } fp8gemm_plan;
 
@@ -124,6 +135,15 @@ typedef struct {
  * Either way bytes past K count as zeros, which adds exactly nothing (the
  * zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
  * paragraph).  Nothing is cached between calls.
+ *
+ * With fp8gemm_options.split_tail on CTA-pair tiles, when the tiles do not
+ * fill the last wave of the persistent grid, that wave's tiles are cut along
+ * K into up to two segments run by different CTA pairs
+ * (fp8gemm_plan.split_tiles).  Every pair then ends after about the same
+ * number of K blocks.  The pair that holds a tile's first K block adds the
+ * other segment's fp32 partial sum (published through the workspace) to its
+ * accumulator, then scales and rounds once, so results do not depend on
+ * timing.  Without a workspace the last wave runs unsplit.
  *
  * Returns FP8GEMM_OK once the kernel is enqueued.  Errors inside the kernel
  * (a bounded wait that ran out) are reported by fp8_gemm_check_device_error.
@@ -147,7 +167,7 @@ int fp8_gemm_plan(int device, const void *x, const void *w, int M, int N, int K,
 
 /*
  * fp8_gemm_workspace_bytes -- device workspace (bytes) a call with these
- * arguments needs for its repitch pass; 0 when it needs none.  x and w are
+ * arguments needs for its repitch pass and split tail; 0 when it needs none.  x and w are
  * used only for their alignment and may be NULL (taken as 16-byte aligned).
  * Returns 0 also for invalid arguments.
  */
@@ -170,8 +190,7 @@ size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M,
  * byte of it that the GEMM then reads, pad bytes included, so nothing has to
  * start at zero.  Calls that need more than that (M * Kp + N * Kp bytes,
  * Kp = round_up(K, 16), each part rounded up to 256 bytes) return
- * FP8GEMM_ESIZE and launch nothing.  Calls that need no repitch launch
- * exactly what fp8_gemm_scaled launches.
+ * FP8GEMM_ESIZE and launch nothing.
  *
  * All calls on a device share the one array and it keeps the last call's
  * contents: two calls that overlap on the GPU (different streams with no

@@ -131,10 +131,14 @@ def test_repitch_equals_in_kernel_loader_bitwise(M, N, K):
     p = fg.plan(M, N, K, Options(path=PATH_MAIN))
     assert p.repitch == 1 and p.launches == 2
     assert p.workspace_bytes >= M * ((K + 15) // 16 * 16) + N * ((K + 15) // 16 * 16)
+    # no split tail: the in-kernel loader runs on one-CTA tiles, whose fp32
+    # sums follow K in the same order as unsplit pair tiles
     a = run(x, w, s, Options(path=PATH_MAIN))
     b = run(x, w, s, Options(path=PATH_MAIN, no_workspace=True))
     assert np.array_equal(a, b)
     compare(a, oracle.linear(x, w, s), f"repitch {M}x{N}x{K}")
+    compare(run(x, w, s, Options(path=PATH_MAIN, split_tail=True)), oracle.linear(x, w, s),
+            f"repitch split {M}x{N}x{K}")
 
 
 def test_caller_workspace():
@@ -152,8 +156,104 @@ def test_caller_workspace():
     with pytest.raises(fg.FP8GemmError) as e:
         fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(workspace=base, workspace_bytes=need - 256))
     assert e.value.status == 1
-    # aligned operands need no workspace
+    # aligned operands need no repitch workspace (only the split tail's, if any)
     assert fg.fp8_gemm_workspace_bytes(torch.cuda.current_device(), M, N, 4096) == 0
+
+
+# ------------------------------------------------------------------ split tail (pair tiles)
+def pairs_on_device():
+    return fg.plan(4096, 4096, 4096, Options(path=PATH_MAIN, mma_ctas=2, tile_n=256)).grid // 2
+
+
+def split_shapes():
+    """Shapes whose last wave is split: no full wave, one full wave plus a
+    few tiles, a ragged M/N/K edge, and few K blocks per tile."""
+    P = pairs_on_device()
+    return [
+        (768, 2048, 1024),            # 24 tiles < P: the whole problem is tail
+        (256 * ((P + 4) // 8 + 1), 2048, 512),  # one full wave, then a short tail
+        (1000, 1500, 1000),           # ragged M, N and K (repitch + split)
+        (512, 512, 256),              # 2 K blocks per tile: tiny segments
+        (2048, 4096, 4096),
+    ]
+
+
+@pytest.mark.parametrize("case", range(5))
+def test_split_tail_matches_oracle(case):
+    M, N, K = split_shapes()[case]
+    opts = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True)
+    p = fg.plan(M, N, K, opts)
+    assert p.split_tiles > 0 and p.tail_workers > p.split_tiles, p
+    assert p.tail_workers <= 2 * p.split_tiles
+    x, w, s = synth.make_inputs(M, N, K, seed=M + N + K)
+    check_full(x, w, s, opts, what=f"split {M}x{N}x{K}")
+
+
+def test_split_tail_exact_sums_and_determinism():
+    # integer operands: the split sums are exact, so split and unsplit tiles
+    # agree bitwise; and a split call gives the same bits every time
+    codes = synth.quantize_e4m3(np.arange(-16, 17, dtype=np.float64))
+    rng = np.random.default_rng(11)
+    M, N, K = 768, 2048, 1024
+    x = rng.choice(codes, (M, K)).astype(np.uint8)
+    w = rng.choice(codes, (N, K)).astype(np.uint8)
+    s = (2.0 ** -rng.integers(0, 12, N)).astype(np.float32)
+    opts = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True)
+    assert fg.plan(M, N, K, opts).split_tiles > 0
+    a = run(x, w, s, opts)
+    b = run(x, w, s, Options(path=PATH_MAIN, mma_ctas=2, tile_n=256))
+    assert fg.plan(M, N, K, Options(path=PATH_MAIN, mma_ctas=2, tile_n=256)).split_tiles == 0
+    assert np.array_equal(a, b)
+    assert np.array_equal(a, oracle.linear(x, w, s))
+    x2, w2, s2 = synth.make_inputs(M, N, K, seed=12)
+    r1 = run(x2, w2, s2, opts)
+    r2 = run(x2, w2, s2, opts)
+    assert np.array_equal(r1, r2)
+
+
+def test_split_tail_caller_workspace_and_stale_flags():
+    # the caller's workspace holds leftovers of an earlier call; the flags are
+    # matched against a per-call value, so the second call must not take the
+    # first call's partial sums
+    M, N, K = 768, 2048, 1024
+    opts = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True)
+    need = fg.fp8_gemm_workspace_bytes(torch.cuda.current_device(), M, N, K, opts)
+    assert need > 0
+    ws = torch.full((need + 512,), 0xFF, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 255) // 256 * 256
+    o2 = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True, workspace=base,
+                 workspace_bytes=need)
+    x, w, s = synth.make_inputs(M, N, K, seed=21)
+    compare(run(x, w, s, o2), oracle.linear(x, w, s), "split caller ws 1")
+    x2, w2, s2 = synth.make_inputs(M, N, K, seed=22)
+    compare(run(x2, w2, s2, o2), oracle.linear(x2, w2, s2), "split caller ws 2")
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    small = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True, workspace=base,
+                    workspace_bytes=need - 256)
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, small)
+    assert e.value.status == 1
+    # without any workspace the last wave runs unsplit
+    assert fg.plan(M, N, K, Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True,
+                                    no_workspace=True)).split_tiles == 0
+    # and it is off unless asked for
+    assert fg.plan(M, N, K, Options(path=PATH_MAIN, mma_ctas=2, tile_n=256)).split_tiles == 0
+
+
+def test_split_tail_back_to_back_on_one_stream():
+    # consecutive split calls share nothing but the stream; each must see its
+    # own partial sums (and the next call may start while this one drains)
+    M, N, K = 768, 2048, 1024
+    opts = Options(path=PATH_MAIN, mma_ctas=2, tile_n=256, split_tail=True)
+    ins = [synth.make_inputs(M, N, K, seed=40 + i) for i in range(4)]
+    dev = [(to_dev(x), to_dev(w), to_dev(s)) for x, w, s in ins]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in ins]
+    for (xd, wd, sd), y in zip(dev, ys):
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, opts)
+    fg.check_device_error()
+    for (x, w, s), y in zip(ins, ys):
+        compare(y_bits(y), oracle.linear(x, w, s), "back to back")
 
 
 # ------------------------------------------------------------------ decode path shapes and tails
