@@ -337,8 +337,14 @@ def run_ours(args):
            "h2d_bytes_per_step": int(x_h.nbytes + w_h.nbytes + s_h.nbytes),
            "d2h_bytes_per_step": int(2 * wl.M * wl.N), "steps": e2e_steps}
 
-    # ---- roofline of the dominant (only) kernel
-    peak_tf = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # ---- roofline of the dominant (only) kernel.  The denominator is the
+    # sustained bf16 figure (x2 for fp8) when the timed region is a long run
+    # of back-to-back launches (power capping then sets the clock, as in the
+    # sustained measurement), the burst figure for a short region.
+    long_region = region_max >= 0.5
+    peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    peak_tf = peaks[peak_key] * FP8_OVER_BF16
+    peak_tf_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
     srcs = DEC_SOURCES if plan.path == fg.PATH_DECODE else TC_SOURCES
     if hbm_metric:
         achieved = wl.algorithmic_bytes / kern / 1e9
@@ -348,9 +354,12 @@ def run_ours(args):
                     "frac_nominal_8000": round(achieved / 8000.0, 4)}
     else:
         achieved = flops / kern / 1e12
+        kind = "sustained" if long_region else "burst"
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_tf, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                    "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} (fp8/bf16 nominal)",
+                    "peak_source": f"{peak_src} bf16 {kind} {peaks[peak_key]} x {FP8_OVER_BF16} "
+                                   f"(fp8/bf16 nominal); timed region {region_max:.2f} s",
+                    "frac_of_burst": round(achieved / peak_tf_burst, 4),
                     "frac_nominal_4500": round(achieved / 4500.0, 4)}
     roofline.update({"traffic": recorded_traffic(key, srcs),
                      "algorithmic_bytes": int(wl.algorithmic_bytes),
@@ -384,7 +393,7 @@ def run_ours(args):
                            "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1),
                            "frac_roofline_nominal": round(roof_t / k2, 4),
                            "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
-                           "frac_fp8_measured": round(tf / peak_tf, 4),
+                           "frac_fp8_measured_burst": round(tf / peak_tf_burst, 4),
                            "path": "main" if p2.path == fg.PATH_MAIN else "decode",
                            "splits": p2.splits, "realign": p2.realign,
                            "l2": "no rotation (launch-bound)" if key2 == "small" else f"rotating {len(sets2)} sets"}
