@@ -59,7 +59,7 @@ struct Cfg2 {
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
   static constexpr int kStgOff = STAGES * kStageBytes;            // 4 warps x 2 staging boxes
   static constexpr int kBarOff = kStgOff + kEpiWarps * 2 * kStgBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5 + kEpiWarps;  // + one per epilogue warp
+  static constexpr int kNumBars = 2 * STAGES + 6 + kEpiWarps;  // + one per epilogue warp
   static constexpr int kPartBytes = BN * 128;  // one warp's share of a partial sum (32 x BN fp32)
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
@@ -70,8 +70,63 @@ struct Cfg2 {
                 "every K block of a stage must start on a 1024-byte swizzle atom");
   static_assert(kEpiWarps * kPartBytes <= STAGES * kStageBytes,
                 "a partial sum must fit in the ring it reuses");
+  // last unit: 8 warps x (up to) half the chunks, one staging box each
+  static constexpr int kHalf = (BN / 32 + 1) / 2;
+  static_assert(2 * kEpiWarps * kHalf * kStgBytes <= STAGES * kStageBytes,
+                "the last unit's staging boxes must fit in the ring");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
+
+// Scale, round and TMA-store accumulator chunks [C0, C1) (32 columns each) of
+// one warp's 32 rows: TMEM address t_row, y rows [row0, row0 + 32), tile
+// column block nb; chunk c is staged in box stg + (c - C0) * kStgBytes, which
+// no earlier store uses.
+template <int BN, int C0, int C1>
+__device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
+                                             const CUtensorMap* tmY, const GemmArgs& p,
+                                             int row0, int nb, uint32_t lane, bool zero_acc) {
+  static_assert(C0 < C1, "chunk range");
+  float scv[C1 - C0];
+#pragma unroll
+  for (int c = C0; c < C1; ++c) {
+    const int col = nb * BN + c * 32 + static_cast<int>(lane);
+    scv[c - C0] = col < p.N ? __ldg(p.scale + col) : 0.f;
+  }
+  uint32_t va[32], vb[32];
+  tmem_ld_32x32b_x32(t_row + C0 * 32, va);
+#pragma unroll
+  for (int c = C0; c < C1; ++c) {
+    tmem_ld_wait();
+    if (c + 1 < C1) {
+      if ((c - C0) & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
+      else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+    }
+    const uint32_t* v = ((c - C0) & 1) ? vb : va;
+    const float sc = scv[c - C0];
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+      const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+      const float a0 = zero_acc ? 0.f : __uint_as_float(v[2 * j]);
+      const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
+      packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
+    }
+    const uint32_t buf = stg + static_cast<uint32_t>(c - C0) * kStgBytes;
+    const uint32_t rb = buf + lane * 64u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+             make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int col0 = nb * BN + c * 32;
+    if (lane == 0) {
+      if (row0 < p.M && col0 < p.N) tma_store_2d(tmY, buf, col0, row0);
+      tma_store_commit();
+    }
+  }
+}
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -92,6 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 4);
   auto part_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + w); };
+  // the epilogue warps' signal that the last unit's accumulator is complete
+  const uint32_t last_bar = bar0 + 8u * (2 * STAGES + 5 + kEpiWarps);
   const uint32_t holder_addr = bar0 + 8u * C::kNumBars;
   volatile uint32_t* holder =
       reinterpret_cast<volatile uint32_t*>(gbase + C::kBarOff + 8 * C::kNumBars);
@@ -117,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(mma_done_bar, 1u);
     for (uint32_t w = 0; w < kEpiWarps; ++w) mbar_init(part_bar(w), 1u);
+    mbar_init(last_bar, static_cast<uint32_t>(kEpiWarps));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -203,6 +261,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    // ---- the last unit's epilogue is exposed (nothing overlaps it), so the
+    // four producer warps, idle by then, store the second half of its chunks
+    // for the 32 rows of their TMEM lane quarter (warp % 4); the epilogue
+    // warps store the first half.  Only for a plain owned tile with a y map.
+    {
+      WorkIter wl(pair, num_pairs, num_tiles, num_kb, tail_workers);
+      WorkUnit u, lu;
+      int n_units = 0;
+      while (wl.next(u)) {
+        lu = u;
+        ++n_units;
+      }
+      if (n_units > 0 && lu.owner && lu.q_end == pair + 1 && p.vec_store) {
+        // the epilogue warps arrive once they have seen the last accumulator
+        // complete (a parity wait on tfull itself could not tell its uses apart)
+        if (mbar_wait_bounded(last_bar, 0u, wc, kErrWaitEpilogue)) {
+          tc_fence_after_sync();
+          int mb, nb;
+          tile_coords(lu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
+          const uint32_t quarter = warp & 3u;
+          const uint32_t acc = static_cast<uint32_t>(n_units - 1) & 1u;
+          const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(quarter) * 32;
+          const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * BN;
+          const uint32_t stg = sbase + (kEpiWarps + (warp - kProdWarp0)) * C::kHalf * kStgBytes;
+          store_chunks<BN, C::kHalf, BN / 32>(t_row, stg, &tmY, p, row0, nb, lane, num_kb == 0);
+          if (lane == 0) tma_store_wait_read<0>();
+          __syncwarp();
+        }
+      }
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (CTA 0)
     if (rank == 0 && lane == 0) {
@@ -270,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
     WorkUnit wu;
     while (wi.next(wu)) {
+      WorkIter peek = wi;
+      WorkUnit nxt;
+      const bool last = !peek.next(nxt);
       int mb, nb;
       tile_coords(wu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
       const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
@@ -278,7 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
       // is used (its registers are read only after the next tcgen05.wait::ld)
       uint32_t va[32], vb[32];
-      if (!wu.owner) {
+      if (last && wu.owner && wu.q_end == pair + 1 && tma_y) {
+        // ---- the last unit, shared with the producer warps (see there): the
+        // operand ring is idle, each chunk gets its own staging box in it
+        if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
+        tc_fence_after_sync();
+        if (lane == 0) mbar_arrive(last_bar);
+        store_chunks<BN, 0, C::kHalf>(t_row, sbase + warp * C::kHalf * kStgBytes, &tmY, p, row0,
+                                      nb, lane, zero_acc);
+      } else if (!wu.owner) {
         // ---- a segment that does not hold the tile's first K block: publish
         // its fp32 partial sum for the owner
         if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
