@@ -14,6 +14,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -441,14 +442,33 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
     const int s_max = std::max(1, std::min(8, num_kb));
     for (int s = 1; s <= s_max; ++s) {
       if (o.splits && s != o.splits) continue;
-      const int clusters = dec_clusters(d, mp, stages, realign, s);
+      // cudaOccupancyMaxActiveClusters answers as if one CTA per SM (the same
+      // count for every ring depth); clusters of CTAs that fit `occ` to an SM
+      // do share SMs (4 splits x 4 stages, 64 clusters of 4 on 152 SMs, ran
+      // in one wave), so the count scales with occ.
+      const int clusters = dec_clusters(d, mp, stages, realign, s) * occ;
       if (clusters <= 0) continue;
+      // The weight stream is shared by the SMs: a wave costs the K blocks of
+      // its busiest SM (CTAs per SM x K blocks per CTA), more when some SMs
+      // stay idle or an SM has less than ~160 KB of loads in flight, plus a
+      // ramp of about five K blocks per wave and about one per split for the
+      // cluster reduction.  (Calibrated on the 32 x 8192 x 8192 decode shape:
+      // 4 splits x 4 stages, 256 CTAs two per SM, 15.2 us; 2 splits x 10
+      // stages, 128 CTAs, 16.4 us; 4 splits x 8 stages, two waves, 21.1 us.)
       const long long waves = (n_tiles + clusters - 1) / clusters;
-      const int per_cta = (num_kb + s - 1) / s;
-      // a wave costs its longest CTA plus a fixed start/reduce cost that grows
-      // with the cluster; shallow rings expose more latency
+      const int per_cta = std::max((num_kb + s - 1) / s, 1);
+      const long long grid = static_cast<long long>(std::min<long long>(n_tiles, clusters)) * s;
+      const int per_sm = static_cast<int>((grid + d.sm_count - 1) / d.sm_count);
+      const double coverage =
+          static_cast<double>(std::min<long long>(grid, d.sm_count)) / d.sm_count;
+      const double in_flight = static_cast<double>(per_sm) * stages *
+                               dec_stage_bytes(mp) / (160.0 * 1024.0);
       const double cost =
-          static_cast<double>(waves) * (std::max(per_cta, 1) + 3.0 + 0.5 * s + 8.0 / stages);
+          static_cast<double>(waves) *
+              (per_cta * per_sm * (1.0 + 0.5 * std::max(0.0, 1.0 - in_flight)) /
+                   std::sqrt(coverage) +
+               5.0) +
+          1.0 * s;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best_s = s;

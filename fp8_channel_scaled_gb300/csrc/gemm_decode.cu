@@ -329,6 +329,8 @@ int dec_threads(bool) { return kThreads; }
 
 int dec_tmem_cols(int mp) { return mp <= 32 ? 32 : (mp <= 64 ? 64 : (mp <= 128 ? 128 : 256)); }
 
+int dec_stage_bytes(int mp) { return (kBN + mp) * kBK; }
+
 cudaError_t dec_prepare(int mp, int stages, bool realign) {
   const DEntry* e = dfind(mp, stages, realign);
   if (!e) return cudaErrorInvalidValue;

@@ -82,6 +82,7 @@ bool dec_config_supported(int mp, int stages, bool realign);
 int dec_smem_bytes(int mp, int stages, bool realign);
 int dec_threads(bool realign);
 int dec_tmem_cols(int mp);
+int dec_stage_bytes(int mp);  // shared-memory bytes of one ring stage (TMA path)
 cudaError_t dec_prepare(int mp, int stages, bool realign);
 cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out);
 cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,
