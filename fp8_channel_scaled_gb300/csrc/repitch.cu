@@ -10,11 +10,15 @@
 // padding only to the next multiple of 16 bytes.  Zero bytes add exactly
 // nothing to a dot product, so results equal the unpadded ones.
 //
-// One thread produces one aligned 16-byte output chunk from the (at most)
-// two aligned 16-byte source words that hold it, so loads and stores are
-// both 16 bytes wide and coalesced along the row; each thread keeps four
-// chunks in flight.  A row holds at most 2^31 / 16 chunks (K < 2^31).  No load touches a 16-byte word that holds no byte of
-// the operand.
+// One warp copies one row of the stacked [x; w] matrix.  Output chunk j of
+// a row (bytes [16 j, 16 j + 16)) is bytes [sh, sh + 16) of the two aligned
+// 16-byte source words at abase + 16 j and abase + 16 (j + 1), where abase
+// is the row start rounded down to 16 bytes and sh the remainder: lane l
+// loads the first word of its chunk, takes the second from lane l + 1 by
+// shuffles (lane 31 loads it), shifts, masks bytes past K and stores 16
+// bytes.  Loads and stores are coalesced along the row, four chunks in
+// flight per lane, and no per-chunk index arithmetic beyond an add.  No
+// load touches a 16-byte word that holds no byte of the row.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "realign.cuh"
@@ -23,54 +27,46 @@ namespace fp8g {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kIlp = 4;
-constexpr int kRowsPerBlock = 8;
+constexpr int kWarps = kThreads / 32;
+constexpr int kU = 4;  // output chunks per lane per iteration
 
-// Each block copies kRowsPerBlock consecutive rows of the stacked [x; w]
-// matrix (M + N rows); its threads walk the rows' 16-byte output chunks with
-// block-local 32-bit indices, kIlp chunks in flight per thread.
 __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) {
   griddep_launch_dependents();
   griddep_wait();
-  const int cpr = a.Kp / 16;  // chunks per row
-  const long long row0 = static_cast<long long>(blockIdx.x) * kRowsPerBlock;
-  const long long rows_total = a.rows_x + a.rows_w;
-  const long long left = rows_total - row0;
-  const int rows_here = left < kRowsPerBlock ? static_cast<int>(left) : kRowsPerBlock;
-  const int units = rows_here * cpr;
-  for (int base = static_cast<int>(threadIdx.x); base < units; base += kThreads * kIlp) {
-    uint4 lo[kIlp], hi[kIlp];
-    uint32_t sh[kIlp];
-    int valid[kIlp];
-    uint8_t* dst[kIlp];
+  const uint32_t lane = threadIdx.x & 31u;
+  const long long r = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (r >= static_cast<long long>(a.rows_x) + a.rows_w) return;
+  const bool is_w = r >= a.rows_x;
+  const long long rr = is_w ? r - a.rows_x : r;
+  const uint8_t* src = (is_w ? a.w : a.x) + rr * a.K;
+  uint8_t* dst = (is_w ? a.wo : a.xo) + rr * a.Kp;
+  const uint32_t sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+  const uint8_t* abase = src - sh;
+  const long long span = static_cast<long long>(sh) + a.K;  // bytes from abase to the row's end
+  const int cpr = a.Kp / 16;                               // output chunks per row
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int j0 = 0; j0 < cpr; j0 += 32 * kU) {
+    uint4 lo[kU];
 #pragma unroll
-    for (int i = 0; i < kIlp; ++i) {
-      const int u = base + i * kThreads;
-      lo[i] = make_uint4(0, 0, 0, 0);
-      hi[i] = make_uint4(0, 0, 0, 0);
-      sh[i] = 0;
-      valid[i] = 0;
-      dst[i] = nullptr;
-      if (u < units) {
-        const int rl = u / cpr;
-        const int kc = 16 * (u - rl * cpr);
-        const long long r = row0 + rl;
-        const bool is_w = r >= a.rows_x;
-        const long long rr = is_w ? r - a.rows_x : r;
-        const uint8_t* src = (is_w ? a.w : a.x) + rr * a.K + kc;
-        dst[i] = (is_w ? a.wo : a.xo) + rr * a.Kp + kc;
-        valid[i] = min(16, a.K - kc);
-        sh[i] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-        const uint8_t* w0 = src - sh[i];
-        lo[i] = ldg_nc_v4(w0);
-        if (sh[i] != 0u && valid[i] > 16 - static_cast<int>(sh[i])) hi[i] = ldg_nc_v4(w0 + 16);
-      }
+    for (int u = 0; u < kU; ++u) {
+      const long long off = 16LL * (j0 + u * 32 + static_cast<int>(lane));
+      lo[u] = off < span ? ldg_nc_v4(abase + off) : zero;
     }
 #pragma unroll
-    for (int i = 0; i < kIlp; ++i) {
-      if (dst[i]) {
-        const uint4 v = keep_bytes(realign16(lo[i], hi[i], sh[i]), valid[i]);
-        *reinterpret_cast<uint4*>(dst[i]) = v;
+    for (int u = 0; u < kU; ++u) {
+      const int j = j0 + u * 32 + static_cast<int>(lane);
+      uint4 hi;
+      hi.x = __shfl_down_sync(0xffffffffu, lo[u].x, 1);
+      hi.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
+      hi.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
+      hi.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
+      if (lane == 31u) {
+        const long long off = 16LL * (j + 1);
+        hi = (sh != 0u && off < span) ? ldg_nc_v4(abase + off) : zero;
+      }
+      if (j < cpr) {
+        const uint4 v = keep_bytes(realign16(lo[u], hi, sh), a.K - 16 * j);
+        *reinterpret_cast<uint4*>(dst + 16LL * j) = v;
       }
     }
   }
@@ -81,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) 
 cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   const long long rows = a.rows_x + a.rows_w;
   if (rows <= 0 || a.Kp <= 0) return cudaSuccess;
-  const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  const long long blocks = (rows + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
