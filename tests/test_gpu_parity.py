@@ -296,6 +296,45 @@ def test_one_hot_weights_reproduce_x_bitwise(path):
     assert np.array_equal(g, r)
 
 
+@pytest.mark.parametrize("path_b", [PATH_MAIN, PATH_DECODE])
+def test_back_to_back_calls_keep_stream_order(path_b):
+    # Consecutive calls on one stream may overlap their launch and set-up
+    # (programmatic dependent launch); every byte they touch must still follow
+    # stream order.  Call A writes y_A; call B reads y_A's bytes as its x
+    # (read after write) and writes its y over A's weight buffer (write after
+    # read).  A's one-hot weight copies small integers into y_A, whose bf16
+    # bytes are then all non-NaN E4M3 codes.
+    ints = np.arange(-8, 9, dtype=np.float64)
+    codes = synth.quantize_e4m3(ints)
+    rng = np.random.default_rng(51)
+    M_A = 64 if path_b == PATH_DECODE else 256
+    K_A = N_A = 512
+    x_a = rng.choice(codes, (M_A, K_A)).astype(np.uint8)
+    w_a = np.zeros((N_A, K_A), np.uint8)
+    w_a[np.arange(N_A), np.arange(K_A)] = 0x38  # 1.0
+    s_a = np.ones(N_A, np.float32)
+    ref_a = oracle.linear(x_a, w_a, s_a)                 # bf16 bits [M_A, N_A]
+    x_b = np.ascontiguousarray(ref_a).view(np.uint8)     # [M_A, 2 N_A] bytes
+    K_B, N_B = 2 * N_A, 256
+    _, w_b, s_b = synth.make_inputs(M_A, N_B, K_B, seed=52)
+    ref_b = oracle.linear(x_b, w_b, s_b)
+    xd_a, sd_a = to_dev(x_a), to_dev(s_a)
+    # A's weight buffer is big enough to hold y_B and is reused for it
+    wbuf = torch.zeros(max(N_A * K_A, 2 * M_A * N_B), dtype=torch.uint8, device="cuda")
+    wbuf[: N_A * K_A].copy_(torch.from_numpy(w_a.reshape(-1)))
+    wd_a = wbuf[: N_A * K_A].view(N_A, K_A)
+    y_a = torch.empty((M_A, N_A), dtype=torch.bfloat16, device="cuda")
+    wd_b, sd_b = to_dev(w_b), to_dev(s_b)
+    y_b = wbuf[: 2 * M_A * N_B].view(torch.bfloat16).view(M_A, N_B)
+    for _ in range(3):
+        wbuf[: N_A * K_A].copy_(torch.from_numpy(w_a.reshape(-1)))
+        fg.fp8_gemm_scaled_ex(xd_a, wd_a, sd_a, y_a, Options(path=PATH_MAIN))
+        fg.fp8_gemm_scaled_ex(y_a.view(torch.uint8), wd_b, sd_b, y_b, Options(path=path_b))
+        fg.check_device_error()
+        assert np.array_equal(y_bits(y_a), ref_a)
+        compare(y_bits(y_b), ref_b, f"chained call, path {path_b}")
+
+
 @pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
 def test_small_integer_operands_bitwise(path):
     # E4M3 codes of the integers -16..16; every partial sum stays an integer
