@@ -33,6 +33,13 @@
  *     padded-input failure, "qwen3.8-max" page, odd-K pad-cache paragraph,
  *     is impossible by construction).
  *   - Thread safety: calls may come from several host threads.
+ *   - CUDA graphs: a call that takes no workspace from the pool (operands
+ *     TMA can tile, or a caller workspace) enqueues kernel launches only and
+ *     can be captured into a graph once the device has been set up by an
+ *     earlier call; replays read the buffers as they are then.  Consecutive
+ *     calls on a stream are launched with programmatic stream serialization:
+ *     each kernel may start its set-up while the previous one drains, and
+ *     touches global memory only after it has completed.
  */
 #ifndef FP8_GEMM_H
 #define FP8_GEMM_H
@@ -63,7 +70,8 @@ typedef enum {
 
 /* Kernel path. */
 enum {
-    FP8GEMM_PATH_AUTO = 0,    /* M <= 64: decode path, else main path */
+    FP8GEMM_PATH_AUTO = 0,    /* M <= 64, or M <= 128 with N <= 8192: decode path,
+                                 else main path */
     FP8GEMM_PATH_MAIN = 1,    /* persistent tcgen05 tile kernel */
     FP8GEMM_PATH_DECODE = 2   /* split-K swap-AB kernel; needs M <= 128 */
 };

@@ -500,3 +500,38 @@ def test_rejects_host_pointers_and_aliasing():
         fg.fp8_gemm_scaled(xa, w, s, ya)
     assert e.value.status == 1
     assert fg.fp8_gemm_check_device_error() == 0
+
+
+# ------------------------------------------------------------------ CUDA graph capture
+@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (512, 1024, 512), (32, 2048, 1024)])
+def test_cuda_graph_capture_and_replay_with_new_data(M, N, K):
+    # A call that needs no workspace enqueues only kernel launches, so it can
+    # be captured into a CUDA graph; a replay recomputes from whatever the
+    # captured buffers hold at that time (nothing is cached).
+    x1, w1, s1 = synth.make_inputs(M, N, K, seed=61)
+    x2, w2, s2 = synth.make_inputs(M, N, K, seed=62)
+    xd, wd, sd = to_dev(x1), to_dev(w1), to_dev(s1)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert fg.plan(M, N, K).workspace_bytes == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fg.fp8_gemm_scaled(xd, wd, sd, y)  # set-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fg.fp8_gemm_scaled(xd, wd, sd, y)
+        fg.fp8_gemm_scaled(xd, wd, sd, y)  # two launches back to back in the graph
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    fg.check_device_error()
+    compare(y_bits(y), oracle.linear(x1, w1, s1), "graph replay 1")
+    xd.copy_(to_dev(x2))
+    wd.copy_(to_dev(w2))
+    sd.copy_(to_dev(s2))
+    g.replay()
+    torch.cuda.synchronize()
+    fg.check_device_error()
+    compare(y_bits(y), oracle.linear(x2, w2, s2), "graph replay 2")
