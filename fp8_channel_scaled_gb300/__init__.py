@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     check_device_error,
     fp8_gemm_check_device_error,
     fp8_gemm_plan,
+    fp8_gemm_prepare_weight,
     fp8_gemm_scaled,
     fp8_gemm_scaled_ex,
     fp8_gemm_scaled_noalloc,

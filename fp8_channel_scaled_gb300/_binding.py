@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import threading
 from dataclasses import dataclass
 from pathlib import Path
@@ -27,7 +28,8 @@ class _COptions(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("splits", ctypes.c_int),
                 ("no_workspace", ctypes.c_int), ("mma_ctas", ctypes.c_int),
                 ("split_tail", ctypes.c_int), ("reserved", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("ldx", ctypes.c_size_t), ("ldw", ctypes.c_size_t)]
 
 
 _PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
@@ -52,6 +54,8 @@ class Options:
     split_tail: bool = False    # share the last partial wave's tiles out by K (needs a workspace)
     workspace: int = 0          # device pointer (e.g. tensor.data_ptr()), 0 = library pool
     workspace_bytes: int = 0
+    ldx: int = 0                # row pitch of x in bytes, 0 = K (set from strided views)
+    ldw: int = 0                # row pitch of w in bytes, 0 = K
 
     def _c(self) -> _COptions:
         o = _COptions()
@@ -62,6 +66,7 @@ class Options:
         o.split_tail = int(bool(self.split_tail))
         o.workspace = int(self.workspace) or None
         o.workspace_bytes = int(self.workspace_bytes)
+        o.ldx, o.ldw = int(self.ldx), int(self.ldw)
         return o
 
 
@@ -107,6 +112,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_scaled.argtypes = [vp, vp, vp, vp, i, i, i, st]
         L.fp8_gemm_scaled_ex.argtypes = [vp, vp, vp, vp, i, i, i, ctypes.POINTER(_COptions), st]
         L.fp8_gemm_scaled_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, st]
+        L.fp8_gemm_prepare_weight.argtypes = [vp, i, i, vp, ctypes.c_size_t, st]
         L.fp8_gemm_plan.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions),
                                     ctypes.POINTER(_CPlan)]
         L.fp8_gemm_workspace_bytes.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions)]
@@ -119,6 +125,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_last_device_error_bits.argtypes = []
         L.fp8_gemm_last_device_error_bits.restype = ctypes.c_uint
         for f in ("fp8_gemm_scaled", "fp8_gemm_scaled_ex", "fp8_gemm_scaled_noalloc",
+                  "fp8_gemm_prepare_weight",
                   "fp8_gemm_plan",
                   "fp8_gemm_check_device_error", "fp8_gemm_set_wait_budget_ns",
                   "fp8_gemm_selftest_wait_timeout", "fp8_gemm_version"):
@@ -146,7 +153,16 @@ def _ptr(t) -> int:
     return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
 
 
-def _shapes(x, w, scale, y):
+def _row_pitch(t, name):
+    """Row pitch (elements) of a 2-D row-major view with unit inner stride."""
+    if t.shape[0] <= 1 or t.is_contiguous():
+        return int(t.shape[1])
+    if t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be row-major with unit inner stride")
+    return int(t.stride(0))
+
+
+def _shapes(x, w, scale, y, strided=False):
     if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
         raise ValueError(f"x {tuple(x.shape)} and w {tuple(w.shape)} must be [M,K] and [N,K]")
     M, K = x.shape
@@ -154,7 +170,9 @@ def _shapes(x, w, scale, y):
     if tuple(scale.shape) != (N,) or tuple(y.shape) != (M, N):
         raise ValueError(f"scale {tuple(scale.shape)} / y {tuple(y.shape)} do not match M={M} N={N}")
     for name, t in (("x", x), ("w", w), ("scale", scale), ("y", y)):
-        if not t.is_contiguous():
+        if strided and name in ("x", "w"):
+            _row_pitch(t, name)
+        elif not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if x.element_size() != 1 or w.element_size() != 1:
         raise TypeError("x and w must be 1-byte E4M3 tensors (uint8 or float8_e4m3fn)")
@@ -177,8 +195,14 @@ def fp8_gemm_scaled(x, w, scale, y, stream=None) -> None:
 
 
 def fp8_gemm_scaled_ex(x, w, scale, y, options: Options | None = None, stream=None) -> None:
-    M, N, K = _shapes(x, w, scale, y)
+    """As fp8_gemm_scaled with options; x and w may be row-major views with a
+    row pitch (e.g. buf[:, :K]): their pitches go to options.ldx / ldw."""
+    M, N, K = _shapes(x, w, scale, y, strided=True)
     o = (options or Options())._c()
+    if not o.ldx and _row_pitch(x, "x") != K:
+        o.ldx = _row_pitch(x, "x")
+    if not o.ldw and _row_pitch(w, "w") != K:
+        o.ldw = _row_pitch(w, "w")
     _check(lib().fp8_gemm_scaled_ex(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
                                     ctypes.byref(o), _stream_handle(stream)), "fp8_gemm_scaled_ex")
 
@@ -190,6 +214,21 @@ def fp8_gemm_scaled_noalloc(x, w, scale, y, stream=None) -> None:
     M, N, K = _shapes(x, w, scale, y)
     _check(lib().fp8_gemm_scaled_noalloc(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
                                          _stream_handle(stream)), "fp8_gemm_scaled_noalloc")
+
+
+def fp8_gemm_prepare_weight(w, w_out, stream=None):
+    """Copy w [N, K] (contiguous) into the rows of w_out, a uint8 [N, ldw]
+    buffer (ldw a multiple of 16, >= K), zeroing bytes past K; returns the
+    [N, K] view of w_out to pass as w (its pitch reaches the library)."""
+    if w.dim() != 2 or not w.is_contiguous() or w.element_size() != 1:
+        raise ValueError("w must be a contiguous 2-D 1-byte tensor")
+    N, K = w.shape
+    if w_out.dim() != 2 or w_out.shape[0] != N or w_out.shape[1] < K or not w_out.is_contiguous():
+        raise ValueError(f"w_out must be a contiguous [{N}, >= {K}] buffer")
+    _check(lib().fp8_gemm_prepare_weight(_ptr(w), int(N), int(K), _ptr(w_out),
+                                         int(w_out.shape[1]), _stream_handle(stream)),
+           "fp8_gemm_prepare_weight")
+    return w_out[:, :K]
 
 
 def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None = None,
@@ -244,7 +283,12 @@ def plan(M: int, N: int, K: int, options: Options | None = None, device: int | N
     if device is None:
         import torch
         device = torch.cuda.current_device()
-    return fp8_gemm_plan(device, M, N, K, options, _ptr(x) if x is not None else 0,
+    o = options or Options()
+    if x is not None and hasattr(x, "stride") and not o.ldx and _row_pitch(x, "x") != K:
+        o = dataclasses.replace(o, ldx=_row_pitch(x, "x"))
+    if w is not None and hasattr(w, "stride") and not o.ldw and _row_pitch(w, "w") != K:
+        o = dataclasses.replace(o, ldw=_row_pitch(w, "w"))
+    return fp8_gemm_plan(device, M, N, K, o, _ptr(x) if x is not None else 0,
                          _ptr(w) if w is not None else 0)
 
 

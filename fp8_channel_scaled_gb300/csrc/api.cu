@@ -245,11 +245,13 @@ int dec_clusters(DevState& d, int mp, int stages, bool realign, int splits) {
   return v;
 }
 
-// TMA descriptor of a row-major byte matrix [rows, K], box [box_rows, 128],
+// TMA descriptor of a byte matrix [rows, K] with row pitch `pitch` (a multiple
+// of 16), box [box_rows, 128],
 // 128-byte swizzle, out-of-bounds elements read as zero.
-int encode_operand(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+int encode_operand(CUtensorMap* map, const void* base, int rows, int K, size_t pitch,
+                   int box_rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
   const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
@@ -277,6 +279,7 @@ struct Plan {
   TcConfig tc;
   DecConfig dec;
   int Kp;                     // row pitch of the repitched operands
+  bool rx, rw;                // x / w repitched into the workspace
   size_t x_off, w_off;        // offsets of the repitched x and w inside the workspace
   size_t part_off, flag_off;  // offsets of the split-tail partial sums and flags
 };
@@ -374,7 +377,15 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   if (o.reserved != 0 || o.mma_ctas < 0 || o.mma_ctas > 2) return FP8GEMM_EINVAL;
   std::memset(pl, 0, sizeof(*pl));
   if (M == 0 || N == 0) return FP8GEMM_OK;  // nothing to do
-  const bool tma_ok = (K % 16 == 0) && (!x || aligned16(x)) && (!w || aligned16(w));
+  const size_t ldx = o.ldx ? o.ldx : static_cast<size_t>(K);
+  const size_t ldw = o.ldw ? o.ldw : static_cast<size_t>(K);
+  if (ldx < static_cast<size_t>(K) || ldw < static_cast<size_t>(K)) return FP8GEMM_EINVAL;
+  // TMA reads an operand in place when its pitch is a multiple of 16 bytes and
+  // its base 16-byte aligned (columns >= K then read as zero)
+  const bool x_tma = (ldx % 16 == 0) && (!x || aligned16(x));
+  const bool w_tma = (ldw % 16 == 0) && (!w || aligned16(w));
+  const bool tma_ok = x_tma && w_tma;
+  const bool contiguous = ldx == static_cast<size_t>(K) && ldw == static_cast<size_t>(K);
   int path = o.path;
   // M <= 64: the decode path.  Up to M = 128 it still wins while the weight
   // is at most 64 n-tiles of 128 rows (measured at N = 4096: M = 96 10.2 vs
@@ -382,22 +393,29 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   if (path == FP8GEMM_PATH_AUTO)
     path = (M <= 64 || (M <= 128 && N <= 64 * 128)) ? FP8GEMM_PATH_DECODE : FP8GEMM_PATH_MAIN;
   if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
-  // Main path with rows TMA cannot tile: repitch into a workspace first,
-  // unless the caller forbids it or asks for the in-kernel loader.
+  // Operands TMA cannot tile are repitched into a workspace first on the main
+  // path (and on the decode path when their pitch is not K, which the
+  // in-kernel loader needs), unless the caller forbids it or asks for the
+  // in-kernel loader.
   const bool can_ws = !o.no_workspace && (o.workspace || !d.pool_failed);
-  const bool repitch = path == FP8GEMM_PATH_MAIN && K > 0 && !tma_ok && !o.force_realign && can_ws;
+  const bool repitch = K > 0 && !tma_ok && !o.force_realign && can_ws &&
+                       (path == FP8GEMM_PATH_MAIN || !contiguous);
   // K == 0 has nothing to load; the realigning variant then issues no copy
   // and needs no tensor map.
   const bool realign = !repitch && (o.force_realign != 0 || !tma_ok || K == 0);
+  if (realign && K > 0 && !contiguous) return FP8GEMM_EALIGN;  // in-kernel loader needs pitch K
   pl->pub.path = path;
   pl->pub.realign = realign ? 1 : 0;
   pl->pub.repitch = repitch ? 1 : 0;
   pl->pub.launches = repitch ? 2 : 1;
   if (repitch) {
     pl->Kp = (K + 15) & ~15;
+    pl->rx = !x_tma;
+    pl->rw = !w_tma;
     pl->x_off = 0;
-    pl->w_off = align256(static_cast<size_t>(M) * pl->Kp);
-    pl->pub.workspace_bytes = pl->w_off + align256(static_cast<size_t>(N) * pl->Kp);
+    pl->w_off = pl->rx ? align256(static_cast<size_t>(M) * pl->Kp) : 0;
+    pl->pub.workspace_bytes =
+        pl->w_off + (pl->rw ? align256(static_cast<size_t>(N) * pl->Kp) : 0);
   }
 
   if (path == FP8GEMM_PATH_MAIN) {
@@ -517,8 +535,11 @@ int pointer_device(const void* p) {
 
 // Enqueue the planned GEMM kernel.  xa / wa are the operands it reads (the
 // caller's, or their repitched copies) with row pitch Ka.
-int launch_gemm(const Plan& pl, DevState& d, const void* xa, const void* wa, int Ka,
-                const float* scale, void* y, int M, int N, uint8_t* ws, cudaStream_t s) {
+// xa / wa (row pitches lxa / lwa) are the operands the kernel reads: the
+// caller's, or their repitched copies; K is the true reduction length.
+int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const void* wa,
+                size_t lwa, int K, const float* scale, void* y, int M, int N, uint8_t* ws,
+                cudaStream_t s) {
   GemmArgs a{};
   a.x = static_cast<const uint8_t*>(xa);
   a.w = static_cast<const uint8_t*>(wa);
@@ -526,8 +547,8 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, const void* wa, int
   a.y = static_cast<uint16_t*>(y);
   a.M = M;
   a.N = N;
-  a.K = Ka;
-  a.num_kb = (Ka + 127) / 128;
+  a.K = K;  // the in-kernel loader (used only with pitch == K) reads rows of K bytes
+  a.num_kb = (K + 127) / 128;
   a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
   a.err = d.err_word;
   a.budget_ns = budget_ns();
@@ -548,13 +569,13 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, const void* wa, int
   CUtensorMap tmA, tmB;
   std::memset(&tmA, 0, sizeof(tmA));
   std::memset(&tmB, 0, sizeof(tmB));
-  const bool use_tma = !pl.pub.realign && Ka > 0;
+  const bool use_tma = !pl.pub.realign && K > 0;
   cudaError_t e;
   if (pl.pub.path == FP8GEMM_PATH_MAIN) {
     // each CTA of a pair loads 128 rows of x and half of the tile's w rows
     const int b_rows = pl.tc.ctas == 2 ? pl.tc.bn / 2 : pl.tc.bn;
-    if (use_tma && (encode_operand(&tmA, xa, M, Ka, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, wa, N, Ka, b_rows) != FP8GEMM_OK))
+    if (use_tma && (encode_operand(&tmA, xa, M, K, lxa, 128) != FP8GEMM_OK ||
+                    encode_operand(&tmB, wa, N, K, lwa, b_rows) != FP8GEMM_OK))
       return FP8GEMM_ELAUNCH;
     if (pl.tc.ctas == 2) {
       CUtensorMap tmY;
@@ -565,8 +586,8 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, const void* wa, int
       e = launch_tc(tmA, tmB, a, pl.tc, s);
     }
   } else {
-    if (use_tma && (encode_operand(&tmA, wa, N, Ka, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, xa, M, Ka, pl.dec.mp) != FP8GEMM_OK))
+    if (use_tma && (encode_operand(&tmA, wa, N, K, lwa, 128) != FP8GEMM_OK ||
+                    encode_operand(&tmB, xa, M, K, lxa, pl.dec.mp) != FP8GEMM_OK))
       return FP8GEMM_ELAUNCH;
     e = launch_decode(tmA, tmB, a, pl.dec, s);
   }
@@ -606,9 +627,10 @@ int noalloc_workspace(DevState& d, uint8_t** out) {
 // Enqueue a planned call whose workspace `ws` (pl.pub.workspace_bytes) is
 // in hand: the repitch copies first, if any, then the GEMM on the operands it
 // reads.
-int run_with_workspace(const Plan& pl, DevState& d, const void* x, const void* w, int K,
-                       const float* scale, void* y, int M, int N, uint8_t* ws, cudaStream_t s) {
-  if (!pl.pub.repitch) return launch_gemm(pl, d, x, w, K, scale, y, M, N, ws, s);
+int run_with_workspace(const Plan& pl, DevState& d, const void* x, size_t ldx, const void* w,
+                       size_t ldw, int K, const float* scale, void* y, int M, int N,
+                       uint8_t* ws, cudaStream_t s) {
+  if (!pl.pub.repitch) return launch_gemm(pl, d, x, ldx, w, ldw, K, scale, y, M, N, ws, s);
   RepitchArgs r{};
   r.x = static_cast<const uint8_t*>(x);
   r.w = static_cast<const uint8_t*>(w);
@@ -616,13 +638,18 @@ int run_with_workspace(const Plan& pl, DevState& d, const void* x, const void* w
   r.wo = ws + pl.w_off;
   r.K = K;
   r.Kp = pl.Kp;
-  r.rows_x = M;
-  r.rows_w = N;
+  r.rows_x = pl.rx ? M : 0;
+  r.rows_w = pl.rw ? N : 0;
+  r.ldx = static_cast<long long>(ldx);
+  r.ldw = static_cast<long long>(ldw);
   if (launch_repitch(r, s) != cudaSuccess) {
     cudaGetLastError();
     return FP8GEMM_ELAUNCH;
   }
-  return launch_gemm(pl, d, r.xo, r.wo, pl.Kp, scale, y, M, N, ws, s);
+  return launch_gemm(pl, d, pl.rx ? static_cast<const void*>(r.xo) : x,
+                     pl.rx ? static_cast<size_t>(pl.Kp) : ldx,
+                     pl.rw ? static_cast<const void*>(r.wo) : w,
+                     pl.rw ? static_cast<size_t>(pl.Kp) : ldw, K, scale, y, M, N, ws, s);
 }
 
 }  // namespace
@@ -638,8 +665,12 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   if (!scale || !y || (K > 0 && (!x || !w))) return FP8GEMM_EINVAL;
   if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(y) & 1u))
     return FP8GEMM_EALIGN;
-  const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K);
-  const size_t wb = static_cast<size_t>(N) * static_cast<size_t>(K);
+  const size_t ldx = (opt && opt->ldx) ? opt->ldx : static_cast<size_t>(K);
+  const size_t ldw = (opt && opt->ldw) ? opt->ldw : static_cast<size_t>(K);
+  if (ldx < static_cast<size_t>(K) || ldw < static_cast<size_t>(K)) return FP8GEMM_EINVAL;
+  // bytes spanned by each operand (the last row is K bytes long)
+  const size_t xb = K > 0 ? (static_cast<size_t>(M) - 1) * ldx + static_cast<size_t>(K) : 0;
+  const size_t wb = K > 0 ? (static_cast<size_t>(N) - 1) * ldw + static_cast<size_t>(K) : 0;
   const size_t yb = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
   const size_t sb = static_cast<size_t>(N) * 4u;
   if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb))
@@ -660,7 +691,7 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   if (st != FP8GEMM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t need = pl.pub.workspace_bytes;
-  if (need == 0) return launch_gemm(pl, *d, x, w, K, scale, y, M, N, nullptr, s);
+  if (need == 0) return launch_gemm(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, nullptr, s);
 
   // workspace (repitch copies and/or split-tail partial sums): the caller's,
   // or stream-ordered from the device's pool
@@ -687,12 +718,12 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
       o2.workspace_bytes = 0;
       st = make_plan(*d, x, w, M, N, K, &o2, &pl);
       if (st != FP8GEMM_OK) return st;
-      return launch_gemm(pl, *d, x, w, K, scale, y, M, N, nullptr, s);
+      return launch_gemm(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, nullptr, s);
     }
     ws = static_cast<uint8_t*>(p);
     pooled = true;
   }
-  st = run_with_workspace(pl, *d, x, w, K, scale, y, M, N, ws, s);
+  st = run_with_workspace(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, ws, s);
   if (pooled && cudaFreeAsync(ws, s) != cudaSuccess) {
     cudaGetLastError();
     if (st == FP8GEMM_OK) st = FP8GEMM_ELAUNCH;
@@ -739,8 +770,42 @@ extern "C" int fp8_gemm_scaled_noalloc(const void* x, const void* w, const float
   st = make_plan(*d, x, w, M, N, K, &o, &pl);
   if (st != FP8GEMM_OK) return st;
   if (pl.pub.workspace_bytes > FP8GEMM_NOALLOC_WORKSPACE_BYTES) return FP8GEMM_ESIZE;
-  return run_with_workspace(pl, *d, x, w, K, scale, y, M, N, ws,
-                            reinterpret_cast<cudaStream_t>(stream));
+  return run_with_workspace(pl, *d, x, static_cast<size_t>(K), w, static_cast<size_t>(K), K,
+                            scale, y, M, N, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_gemm_prepare_weight(const void* w, int N, int K, void* w_out,
+                                       size_t ldw_out, fp8gemm_stream_t stream) {
+  if (N < 0 || K < 0) return FP8GEMM_EINVAL;
+  if (N == 0 || K == 0) return FP8GEMM_OK;
+  if (!w || !w_out || ldw_out < static_cast<size_t>(K)) return FP8GEMM_EINVAL;
+  if ((ldw_out % 16u) != 0 || (reinterpret_cast<uintptr_t>(w_out) & 15u)) return FP8GEMM_EALIGN;
+  if (ldw_out > 0x7FFFFFFFu) return FP8GEMM_EINVAL;
+  const size_t wb = static_cast<size_t>(N) * static_cast<size_t>(K);
+  const size_t ob = (static_cast<size_t>(N) - 1) * ldw_out + ldw_out;
+  if (overlaps(w, wb, w_out, ob)) return FP8GEMM_EINVAL;
+  const int dev = pointer_device(w_out);
+  if (dev < 0 || pointer_device(w) != dev) return FP8GEMM_EINVAL;
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  RepitchArgs r{};
+  r.w = static_cast<const uint8_t*>(w);
+  r.wo = static_cast<uint8_t*>(w_out);
+  r.K = K;
+  r.Kp = static_cast<int>(ldw_out);
+  r.rows_x = 0;
+  r.rows_w = N;
+  r.ldw = K;
+  if (launch_repitch(r, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  return FP8GEMM_OK;
 }
 
 extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,

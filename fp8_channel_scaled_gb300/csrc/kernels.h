@@ -93,13 +93,14 @@ cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
 
 // ---- repitch of unaligned operands into a workspace ------------------------
 struct RepitchArgs {
-  const uint8_t* x;      // [M, K], any alignment
-  const uint8_t* w;      // [N, K], any alignment
-  uint8_t* xo;           // [M, Kp], 16-byte aligned
-  uint8_t* wo;           // [N, Kp], 16-byte aligned
-  int K, Kp;             // Kp = round_up(K, 16)
-  long long rows_x;      // M
-  long long rows_w;      // N
+  const uint8_t* x;      // [rows_x, K] with row pitch ldx bytes, any alignment
+  const uint8_t* w;      // [rows_w, K] with row pitch ldw bytes, any alignment
+  uint8_t* xo;           // [rows_x, Kp], 16-byte aligned
+  uint8_t* wo;           // [rows_w, Kp], 16-byte aligned
+  int K, Kp;             // Kp = a multiple of 16 >= K; bytes [K, Kp) of each row are set to 0
+  long long rows_x;      // M, or 0 to leave x alone
+  long long rows_w;      // N, or 0 to leave w alone
+  long long ldx, ldw;    // source row pitches (>= K)
 };
 cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s);
 

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) 
   if (r >= static_cast<long long>(a.rows_x) + a.rows_w) return;
   const bool is_w = r >= a.rows_x;
   const long long rr = is_w ? r - a.rows_x : r;
-  const uint8_t* src = (is_w ? a.w : a.x) + rr * a.K;
+  const uint8_t* src = (is_w ? a.w : a.x) + rr * (is_w ? a.ldw : a.ldx);
   uint8_t* dst = (is_w ? a.wo : a.xo) + rr * a.Kp;
   const uint32_t sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
   const uint8_t* abase = src - sh;

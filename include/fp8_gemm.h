@@ -54,7 +54,7 @@ extern "C" {
  * (identical to cudaStream_t). */
 typedef struct CUstream_st *fp8gemm_stream_t;
 
-#define FP8GEMM_VERSION 2
+#define FP8GEMM_VERSION 3
 
 typedef enum {
     FP8GEMM_OK = 0,
@@ -99,6 +99,13 @@ typedef struct {
     int reserved;       /* must be zero */
     void *workspace;    /* optional caller workspace (device, 256-byte aligned) */
     size_t workspace_bytes; /* its size; must be >= fp8_gemm_workspace_bytes() */
+    size_t ldx;         /* row pitch of x in bytes (0 = K): row m starts at x + m * ldx;
+                           the caller guarantees [x, x + (M-1)*ldx + K) is device memory */
+    size_t ldw;         /* row pitch of w in bytes (0 = K).  An operand whose pitch is a
+                           multiple of 16 and whose base is 16-byte aligned is read in
+                           place by TMA whatever K is (bytes past K in a row are never
+                           read); any other operand is repitched into the workspace
+                           (or, with pitch == K, loaded by the realigning producer) */
 } fp8gemm_options;
 
 /* What a call with the same arguments would launch (see fp8_gemm_plan). */
@@ -213,6 +220,20 @@ size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M,
 #define FP8GEMM_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 int fp8_gemm_scaled_noalloc(const void *x, const void *w, const float *scale, void *y,
                             int M, int N, int K, fp8gemm_stream_t stream);
+
+/*
+ * fp8_gemm_prepare_weight -- copy w [N, K] (row pitch K, any alignment) to
+ * w_out with row pitch ldw_out (a multiple of 16, >= K; w_out 16-byte
+ * aligned), bytes [K, ldw_out) of each row set to zero.  Passing w_out with
+ * fp8gemm_options.ldw = ldw_out then lets every later call read the weight
+ * with TMA in place, so that only x is repitched per call when K % 16 != 0
+ * (the pages cache a padded weight per weight version: "glm-5.2" page,
+ * Triton TMA paragraph; "Kimi K3 (256k)" page, sm_100 tcgen05 paragraph;
+ * here the caller owns the copy and decides when it is stale, and the
+ * default path keeps nothing between calls).  Asynchronous on `stream`; w_out must not overlap w.
+ */
+int fp8_gemm_prepare_weight(const void *w, int N, int K, void *w_out, size_t ldw_out,
+                            fp8gemm_stream_t stream);
 
 /*
  * fp8_gemm_check_device_error -- synchronise `stream`, read and clear the

@@ -535,3 +535,85 @@ def test_cuda_graph_capture_and_replay_with_new_data(M, N, K):
     torch.cuda.synchronize()
     fg.check_device_error()
     compare(y_bits(y), oracle.linear(x2, w2, s2), "graph replay 2")
+
+
+# ------------------------------------------------------------------ operand pitches, weight prepack
+def pitched(a, pitch, fill=0xA5):
+    """Device copy of a [rows, K] byte matrix inside a [rows, pitch] buffer
+    (bytes past K poisoned), returned as the [rows, K] view."""
+    rows, K = a.shape
+    buf = np.full((rows, pitch), fill, np.uint8)
+    buf[:, :K] = a
+    return to_dev(buf)[:, :K]
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_pitched_operands_read_in_place(path):
+    # pitch a multiple of 16 with K = 4127: TMA reads the operands where they
+    # are (no workspace, one launch); bytes past K are never used
+    M = 32 if path == PATH_DECODE else 300
+    N, K, P = 520, 4127, 4144
+    x, w, s = synth.make_inputs(M, N, K, seed=71)
+    xv, wv = pitched(x, P), pitched(w, P)
+    p = fg.plan(M, N, K, Options(path=path), x=xv, w=wv)
+    assert p.workspace_bytes == 0 and p.launches == 1 and p.repitch == 0 and p.realign == 0
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_scaled_ex(xv, wv, to_dev(s), y, Options(path=path))
+    fg.check_device_error()
+    got = y_bits(y)
+    compare(got, oracle.linear(x, w, s), f"pitched {path}")
+    if path == PATH_MAIN:  # same K blocks and zeros as the repitched contiguous call
+        assert np.array_equal(got, run(x, w, s, Options(path=path)))
+
+
+@pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
+def test_pitched_operands_unaligned_pitch_are_repitched(path):
+    M = 40 if path == PATH_DECODE else 260
+    N, K, P = 300, 1000, 1013
+    x, w, s = synth.make_inputs(M, N, K, seed=72)
+    xv, wv = pitched(x, P), pitched(w, P)
+    p = fg.plan(M, N, K, Options(path=path), x=xv, w=wv)
+    assert p.repitch == 1 and p.launches == 2
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_scaled_ex(xv, wv, to_dev(s), y, Options(path=path))
+    fg.check_device_error()
+    compare(y_bits(y), oracle.linear(x, w, s), f"unaligned pitch {path}")
+    # without a workspace the in-kernel loader cannot follow a pitch != K
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled_ex(xv, wv, to_dev(s), y, Options(path=path, no_workspace=True))
+    assert e.value.status == 2
+
+
+def test_prepare_weight_leaves_only_x_to_repitch():
+    M, N, K = 512, 1024, 4127
+    x, w, s = synth.make_inputs(M, N, K, seed=73)
+    wd = to_dev(w)
+    w_out = torch.full((N, 4128), 0x5A, dtype=torch.uint8, device="cuda")
+    wv = fg.fp8_gemm_prepare_weight(wd, w_out)
+    torch.cuda.synchronize()
+    host = w_out.cpu().numpy()
+    assert np.array_equal(host[:, :K], w) and not host[:, K:].any()
+    p_full = fg.plan(M, N, K, x=to_dev(x), w=wd)
+    p_prep = fg.plan(M, N, K, x=to_dev(x), w=wv)
+    assert p_prep.repitch == 1 and p_prep.workspace_bytes < p_full.workspace_bytes
+    assert p_prep.workspace_bytes == (M * 4128 + 255) // 256 * 256
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_scaled_ex(to_dev(x), wv, to_dev(s), y)
+    fg.check_device_error()
+    got = y_bits(y)
+    assert np.array_equal(got, run(x, w, s))
+    compare(got, oracle.linear(x, w, s), "prepared weight")
+
+
+def test_pitch_arguments_are_checked():
+    M, N, K = 64, 128, 256
+    x, w, s = synth.make_inputs(M, N, K, seed=74)
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(ldx=K - 1))
+    assert e.value.status == 1
+    out = torch.empty((N, 264), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fg.FP8GemmError) as e:  # ldw_out not a multiple of 16
+        fg.fp8_gemm_prepare_weight(wd, out)
+    assert e.value.status == 2
