@@ -10,15 +10,16 @@
 // padding only to the next multiple of 16 bytes.  Zero bytes add exactly
 // nothing to a dot product, so results equal the unpadded ones.
 //
-// One warp copies one row of the stacked [x; w] matrix.  Output chunk j of
-// a row (bytes [16 j, 16 j + 16)) is bytes [sh, sh + 16) of the two aligned
-// 16-byte source words at abase + 16 j and abase + 16 (j + 1), where abase
-// is the row start rounded down to 16 bytes and sh the remainder: lane l
-// loads the first word of its chunk, takes the second from lane l + 1 by
-// shuffles (lane 31 loads it), shifts, masks bytes past K and stores 16
-// bytes.  Loads and stores are coalesced along the row, four chunks in
-// flight per lane, and no per-chunk index arithmetic beyond an add.  No
-// load touches a 16-byte word that holds no byte of the row.
+// One warp copies a segment of 64 output chunks (1 KiB) of one row of the
+// stacked [x; w] matrix, so that even a copy of a few thousand rows has tens
+// of thousands of loads in flight at once.  Output chunk j of a row (bytes
+// [16 j, 16 j + 16)) is bytes [sh, sh + 16) of the two aligned 16-byte source
+// words at abase + 16 j and abase + 16 (j + 1), where abase is the row start
+// rounded down to 16 bytes and sh the remainder: lane l loads the first word
+// of its chunk, takes the second from lane l + 1 by shuffles (lane 31 loads
+// it), shifts, masks bytes past K and stores 16 bytes.  Loads and stores are
+// coalesced along the row.  No load touches a 16-byte word that holds no byte
+// of the row.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "realign.cuh"
@@ -28,14 +29,18 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kU = 4;  // output chunks per lane per iteration
+constexpr int kU = 2;                // output chunks per lane
+constexpr int kSegChunks = 32 * kU;  // output chunks per warp
 
-__global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) {
+__global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a,
+                                                           const int segs_per_row) {
   griddep_launch_dependents();
   griddep_wait();
   const uint32_t lane = threadIdx.x & 31u;
-  const long long r = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (r >= static_cast<long long>(a.rows_x) + a.rows_w) return;
+  const long long g = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const long long r = g / segs_per_row;
+  if (r >= a.rows_x + a.rows_w) return;
+  const int j0 = static_cast<int>(g - r * segs_per_row) * kSegChunks;
   const bool is_w = r >= a.rows_x;
   const long long rr = is_w ? r - a.rows_x : r;
   const uint8_t* src = (is_w ? a.w : a.x) + rr * (is_w ? a.ldw : a.ldx);
@@ -45,29 +50,27 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) 
   const long long span = static_cast<long long>(sh) + a.K;  // bytes from abase to the row's end
   const int cpr = a.Kp / 16;                               // output chunks per row
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  for (int j0 = 0; j0 < cpr; j0 += 32 * kU) {
-    uint4 lo[kU];
+  uint4 lo[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const long long off = 16LL * (j0 + u * 32 + static_cast<int>(lane));
-      lo[u] = off < span ? ldg_nc_v4(abase + off) : zero;
+  for (int u = 0; u < kU; ++u) {
+    const long long off = 16LL * (j0 + u * 32 + static_cast<int>(lane));
+    lo[u] = off < span ? ldg_nc_v4(abase + off) : zero;
+  }
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    const int j = j0 + u * 32 + static_cast<int>(lane);
+    uint4 hi;
+    hi.x = __shfl_down_sync(0xffffffffu, lo[u].x, 1);
+    hi.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
+    hi.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
+    hi.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
+    if (lane == 31u) {
+      const long long off = 16LL * (j + 1);
+      hi = (sh != 0u && off < span) ? ldg_nc_v4(abase + off) : zero;
     }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int j = j0 + u * 32 + static_cast<int>(lane);
-      uint4 hi;
-      hi.x = __shfl_down_sync(0xffffffffu, lo[u].x, 1);
-      hi.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
-      hi.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
-      hi.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
-      if (lane == 31u) {
-        const long long off = 16LL * (j + 1);
-        hi = (sh != 0u && off < span) ? ldg_nc_v4(abase + off) : zero;
-      }
-      if (j < cpr) {
-        const uint4 v = keep_bytes(realign16(lo[u], hi, sh), a.K - 16 * j);
-        *reinterpret_cast<uint4*>(dst + 16LL * j) = v;
-      }
+    if (j < cpr) {
+      const uint4 v = keep_bytes(realign16(lo[u], hi, sh), a.K - 16 * j);
+      *reinterpret_cast<uint4*>(dst + 16LL * j) = v;
     }
   }
 }
@@ -77,7 +80,8 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a) 
 cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   const long long rows = a.rows_x + a.rows_w;
   if (rows <= 0 || a.Kp <= 0) return cudaSuccess;
-  const long long blocks = (rows + kWarps - 1) / kWarps;
+  const int segs = (a.Kp / 16 + kSegChunks - 1) / kSegChunks;
+  const long long blocks = (rows * segs + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
@@ -87,7 +91,7 @@ cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   set_pdl(attr[0]);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, repitch_kernel, a);
+  return cudaLaunchKernelEx(&cfg, repitch_kernel, a, segs);
 }
 
 }  // namespace fp8g
