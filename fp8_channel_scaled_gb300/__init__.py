@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     STATUS,
     check_device_error,
     fp8_gemm_check_device_error,
+    fp8_gemm_grouped,
     fp8_gemm_plan,
     fp8_gemm_prepare_weight,
     fp8_gemm_scaled,

@@ -113,6 +113,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_scaled_ex.argtypes = [vp, vp, vp, vp, i, i, i, ctypes.POINTER(_COptions), st]
         L.fp8_gemm_scaled_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, st]
         L.fp8_gemm_prepare_weight.argtypes = [vp, i, i, vp, ctypes.c_size_t, st]
+        L.fp8_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(_COptions), st]
         L.fp8_gemm_plan.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions),
                                     ctypes.POINTER(_CPlan)]
         L.fp8_gemm_workspace_bytes.argtypes = [i, vp, vp, i, i, i, ctypes.POINTER(_COptions)]
@@ -125,7 +126,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_last_device_error_bits.argtypes = []
         L.fp8_gemm_last_device_error_bits.restype = ctypes.c_uint
         for f in ("fp8_gemm_scaled", "fp8_gemm_scaled_ex", "fp8_gemm_scaled_noalloc",
-                  "fp8_gemm_prepare_weight",
+                  "fp8_gemm_prepare_weight", "fp8_gemm_grouped",
                   "fp8_gemm_plan",
                   "fp8_gemm_check_device_error", "fp8_gemm_set_wait_budget_ns",
                   "fp8_gemm_selftest_wait_timeout", "fp8_gemm_version"):
@@ -214,6 +215,29 @@ def fp8_gemm_scaled_noalloc(x, w, scale, y, stream=None) -> None:
     M, N, K = _shapes(x, w, scale, y)
     _check(lib().fp8_gemm_scaled_noalloc(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
                                          _stream_handle(stream)), "fp8_gemm_scaled_noalloc")
+
+
+def fp8_gemm_grouped(x, w, scale, y, offsets, options: Options | None = None, stream=None) -> None:
+    """Grouped layer: x [M, K], w [G, N, K], scale [G, N], y [M, N], offsets
+    int32 [G + 1] on the device (group g owns rows offsets[g] .. offsets[g+1])."""
+    if x.dim() != 2 or w.dim() != 3 or scale.dim() != 2 or y.dim() != 2 or offsets.dim() != 1:
+        raise ValueError("x [M,K], w [G,N,K], scale [G,N], y [M,N], offsets [G+1] expected")
+    M, K = x.shape
+    G, N, Kw = w.shape
+    if Kw != K or tuple(scale.shape) != (G, N) or tuple(y.shape) != (M, N) or offsets.shape[0] != G + 1:
+        raise ValueError("shapes do not match")
+    for name, t in (("w", w), ("scale", scale), ("y", y), ("offsets", offsets)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if x.element_size() != 1 or w.element_size() != 1 or scale.element_size() != 4 \
+            or y.element_size() != 2 or offsets.element_size() != 4:
+        raise TypeError("x, w: 1-byte E4M3; scale: float32; y: bfloat16; offsets: int32")
+    o = (options or Options())._c()
+    if not o.ldx and _row_pitch(x, "x") != K:
+        o.ldx = _row_pitch(x, "x")
+    _check(lib().fp8_gemm_grouped(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), _ptr(offsets), int(G),
+                                  int(M), int(N), int(K), ctypes.byref(o), _stream_handle(stream)),
+           "fp8_gemm_grouped")
 
 
 def fp8_gemm_prepare_weight(w, w_out, stream=None):

@@ -539,7 +539,7 @@ int pointer_device(const void* p) {
 // caller's, or their repitched copies; K is the true reduction length.
 int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const void* wa,
                 size_t lwa, int K, const float* scale, void* y, int M, int N, uint8_t* ws,
-                cudaStream_t s) {
+                cudaStream_t s, const int* group_offsets = nullptr, int groups = 0) {
   GemmArgs a{};
   a.x = static_cast<const uint8_t*>(xa);
   a.w = static_cast<const uint8_t*>(wa);
@@ -552,6 +552,10 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const v
   a.vec_store = ((N % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0) ? 1 : 0;
   a.err = d.err_word;
   a.budget_ns = budget_ns();
+  a.group_offsets = group_offsets;
+  a.groups = groups;
+  // a grouped layer's weight is [groups * N, K]
+  const int w_rows = group_offsets ? groups * N : N;
   if (pl.pub.path == FP8GEMM_PATH_MAIN && pl.tc.tail_workers > 0) {
     if (!ws) return FP8GEMM_EINVAL;
     a.tail_workers = pl.tc.tail_workers;
@@ -575,7 +579,7 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const v
     // each CTA of a pair loads 128 rows of x and half of the tile's w rows
     const int b_rows = pl.tc.ctas == 2 ? pl.tc.bn / 2 : pl.tc.bn;
     if (use_tma && (encode_operand(&tmA, xa, M, K, lxa, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, wa, N, K, lwa, b_rows) != FP8GEMM_OK))
+                    encode_operand(&tmB, wa, w_rows, K, lwa, b_rows) != FP8GEMM_OK))
       return FP8GEMM_ELAUNCH;
     if (pl.tc.ctas == 2) {
       CUtensorMap tmY;
@@ -806,6 +810,65 @@ extern "C" int fp8_gemm_prepare_weight(const void* w, int N, int K, void* w_out,
     return FP8GEMM_ELAUNCH;
   }
   return FP8GEMM_OK;
+}
+
+extern "C" int fp8_gemm_grouped(const void* x, const void* w, const float* scale, void* y,
+                                const int* offsets, int groups, int M, int N, int K,
+                                const fp8gemm_options* opt, fp8gemm_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || groups < 0) return FP8GEMM_EINVAL;
+  if (M == 0 || N == 0 || groups == 0) return FP8GEMM_OK;
+  if (K == 0 || !x || !w || !scale || !y || !offsets) return FP8GEMM_EINVAL;
+  if (static_cast<long long>(groups) * N > 0x7FFFFFFFLL) return FP8GEMM_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(y) & 1u) ||
+      (reinterpret_cast<uintptr_t>(offsets) & 3u))
+    return FP8GEMM_EALIGN;
+  const size_t ldx = (opt && opt->ldx) ? opt->ldx : static_cast<size_t>(K);
+  const size_t ldw = (opt && opt->ldw) ? opt->ldw : static_cast<size_t>(K);
+  if (ldx < static_cast<size_t>(K) || ldw < static_cast<size_t>(K)) return FP8GEMM_EINVAL;
+  const long long w_rows = static_cast<long long>(groups) * N;
+  const size_t xb = (static_cast<size_t>(M) - 1) * ldx + static_cast<size_t>(K);
+  const size_t wb = (static_cast<size_t>(w_rows) - 1) * ldw + static_cast<size_t>(K);
+  const size_t yb = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
+  const size_t sb = static_cast<size_t>(w_rows) * 4u;
+  const size_t ob = (static_cast<size_t>(groups) + 1u) * 4u;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb) ||
+      overlaps(y, yb, offsets, ob))
+    return FP8GEMM_EINVAL;
+  const int dev = pointer_device(y);
+  if (dev < 0 || pointer_device(scale) != dev || pointer_device(x) != dev ||
+      pointer_device(w) != dev || pointer_device(offsets) != dev)
+    return FP8GEMM_EINVAL;
+  DevState* d = nullptr;
+  int st = device_state(dev, &d);
+  if (st != FP8GEMM_OK) return st;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  // CTA-pair tiles chosen as for one group of M rows; the work list (tiles of
+  // every group) is built on the device, so every resident pair is launched.
+  fp8gemm_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (o.path == FP8GEMM_PATH_DECODE || o.mma_ctas == 1 || o.force_realign) return FP8GEMM_EUNSUPPORTED;
+  // the grouped layer reads its operands with TMA only
+  if ((ldx % 16) || (ldw % 16) || !aligned16(x) || !aligned16(w)) return FP8GEMM_EALIGN;
+  o.path = FP8GEMM_PATH_MAIN;
+  o.mma_ctas = 2;
+  o.split_tail = 0;
+  o.no_workspace = 1;
+  o.workspace = nullptr;
+  o.workspace_bytes = 0;
+  Plan pl;
+  st = make_plan(*d, x, w, M, N, K, &o, &pl);
+  if (st != FP8GEMM_OK) return st;
+  if (pl.pub.realign || pl.pub.repitch) return FP8GEMM_EALIGN;
+  const int pairs = tc2_pairs(*d, pl.tc.bn, pl.tc.stages);
+  if (pairs <= 0) return FP8GEMM_ELAUNCH;
+  pl.tc.grid = 2 * pairs;
+  pl.tc.tail_workers = 0;
+  return launch_gemm(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), offsets, groups);
 }
 
 extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale, void* y, int M,

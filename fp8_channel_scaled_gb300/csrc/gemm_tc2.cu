@@ -77,20 +77,50 @@ struct Cfg2 {
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// Scale, round and TMA-store accumulator chunks [C0, C1) (32 columns each) of
-// one warp's 32 rows: TMEM address t_row, y rows [row0, row0 + 32), tile
-// column block nb; chunk c is staged in box stg + (c - C0) * kStgBytes, which
-// no earlier store uses.
+// Write one staged 32 x 32 chunk of y (lane l holds row row0 + l, columns
+// col0 .. col0 + 31, as 16 packed bf16 pairs): one lane TMA-stores the box
+// when every row of it is this tile's (rows past M are clipped by the
+// store); when the box straddles the end of the tile's group, each lane
+// stores its own row, if it is the group's, from registers.  A (possibly
+// empty) bulk group is committed either way, so that staging-box accounting
+// always refers to the same chunk.  Needs 16-byte y rows (vec_store).
+__device__ __forceinline__ void emit_chunk(const CUtensorMap* tmY, uint32_t buf,
+                                           const GemmArgs& p, int row0, int row_end, int col0,
+                                           uint32_t lane, const uint32_t* packed) {
+  const bool whole = row0 + 32 <= row_end || row_end >= p.M;
+  if (lane == 0) {
+    if (whole && row0 < p.M && col0 < p.N) tma_store_2d(tmY, buf, col0, row0);
+    tma_store_commit();
+  }
+  if (!whole) {
+    const int row = row0 + static_cast<int>(lane);
+    if (row < row_end && row < p.M) {
+      uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (col0 + 8 * q < p.N)
+          dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                              packed[4 * q + 3]);
+    }
+  }
+}
+
+// Scale, round and store accumulator chunks [C0, C1) (32 columns each) of
+// one warp's 32 rows: TMEM address t_row, y rows [row0, row0 + 32) of which
+// those below row_end are the tile's, tile column block nb, scales from
+// scale[sbase + column]; chunk c is staged in box stg + (c - C0) * kStgBytes,
+// which no earlier store uses.
 template <int BN, int C0, int C1>
 __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
                                              const CUtensorMap* tmY, const GemmArgs& p,
-                                             int row0, int nb, uint32_t lane, bool zero_acc) {
+                                             int row0, int row_end, int nb, int sbase,
+                                             uint32_t lane, bool zero_acc) {
   static_assert(C0 < C1, "chunk range");
   float scv[C1 - C0];
 #pragma unroll
   for (int c = C0; c < C1; ++c) {
     const int col = nb * BN + c * 32 + static_cast<int>(lane);
-    scv[c - C0] = col < p.N ? __ldg(p.scale + col) : 0.f;
+    scv[c - C0] = col < p.N ? __ldg(p.scale + sbase + col) : 0.f;
   }
   uint32_t va[32], vb[32];
   tmem_ld_32x32b_x32(t_row + C0 * 32, va);
@@ -120,11 +150,7 @@ __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
              make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]));
     fence_proxy_async_smem();
     __syncwarp();
-    const int col0 = nb * BN + c * 32;
-    if (lane == 0) {
-      if (row0 < p.M && col0 < p.N) tma_store_2d(tmY, buf, col0, row0);
-      tma_store_commit();
-    }
+    emit_chunk(tmY, buf, p, row0, row_end, nb * BN + c * 32, lane, packed);
   }
 }
 
@@ -202,7 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
 
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
-  const int num_tiles = num_m2_blk * num_n_blk;
+  // a fresh mapper per role: each walks the tile list forward once
+  auto mapper = [&]() {
+    return TileMapper(p.group_offsets, p.groups, p.M, p.N, BN, num_n_blk, num_m2_blk, group_m);
+  };
+  const int num_tiles = static_cast<int>(mapper().total());
   const int num_kb = p.num_kb;
   const int tail_workers = p.tail_workers;
 
@@ -223,11 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
       WorkUnit wu;
+      TileMapper tm = mapper();
       while (ok && wi.next(wu)) {
-        int mb, nb;
-        tile_coords(wu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
-        const int row = is_a ? mb * 256 + static_cast<int>(rank) * 128
-                             : nb * BN + static_cast<int>(rank) * C::kBRows;
+        const TileGeom tg = tm.at(wu.tile);
+        const int row = is_a ? tg.row + static_cast<int>(rank) * 128
+                             : tg.wrow + static_cast<int>(rank) * C::kBRows;
         for (int kb = wu.k0; kb < wu.k1; kb += kKbPerStage, ++it) {
           if (kKbPerStage == 1 && static_cast<int>(it & 1u) != sub) continue;
           const uint32_t stage = it % STAGES;
@@ -278,14 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // complete (a parity wait on tfull itself could not tell its uses apart)
         if (mbar_wait_bounded(last_bar, 0u, wc, kErrWaitEpilogue)) {
           tc_fence_after_sync();
-          int mb, nb;
-          tile_coords(lu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
+          TileMapper tm = mapper();
+          const TileGeom tg = tm.at(lu.tile);
           const uint32_t quarter = warp & 3u;
           const uint32_t acc = static_cast<uint32_t>(n_units - 1) & 1u;
-          const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(quarter) * 32;
+          const int row0 = tg.row + static_cast<int>(rank) * 128 + static_cast<int>(quarter) * 32;
           const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * BN;
           const uint32_t stg = sbase + (kEpiWarps + (warp - kProdWarp0)) * C::kHalf * kStgBytes;
-          store_chunks<BN, C::kHalf, BN / 32>(t_row, stg, &tmY, p, row0, nb, lane, num_kb == 0);
+          store_chunks<BN, C::kHalf, BN / 32>(t_row, stg, &tmY, p, row0, tg.row_end, tg.nb,
+                                              tg.sbase, lane, num_kb == 0);
           if (lane == 0) tma_store_wait_read<0>();
           __syncwarp();
         }
@@ -357,13 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     WorkIter wi(pair, num_pairs, num_tiles, num_kb, tail_workers);
     WorkUnit wu;
+    TileMapper tm = mapper();
     while (wi.next(wu)) {
       WorkIter peek = wi;
       WorkUnit nxt;
       const bool last = !peek.next(nxt);
-      int mb, nb;
-      tile_coords(wu.tile, num_m2_blk, num_n_blk, group_m, mb, nb);
-      const int row0 = mb * 256 + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
+      const TileGeom tg = tm.at(wu.tile);
+      const int nb = tg.nb;
+      const int row0 = tg.row + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
       const int row = row0 + static_cast<int>(lane);
       const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
       // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
@@ -376,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         if (lane == 0) mbar_arrive(last_bar);
         store_chunks<BN, 0, C::kHalf>(t_row, sbase + warp * C::kHalf * kStgBytes, &tmY, p, row0,
-                                      nb, lane, zero_acc);
+                                      tg.row_end, nb, tg.sbase, lane, zero_acc);
       } else if (!wu.owner) {
         // ---- a segment that does not hold the tile's first K block: publish
         // its fp32 partial sum for the owner
@@ -407,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
           const int col = nb * BN + c * 32 + static_cast<int>(lane);
-          scv[c] = col < p.N ? __ldg(p.scale + col) : 0.f;
+          scv[c] = col < p.N ? __ldg(p.scale + tg.sbase + col) : 0.f;
         }
         if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
         tc_fence_after_sync();
@@ -484,14 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 packed[4 * q + 3]));
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-              // boxes entirely past M or N are not issued; the (possibly empty)
-              // group is committed either way so that the buffer accounting
-              // above always refers to the same chunk
-              if (row0 < p.M && col0 < p.N) tma_store_2d(&tmY, buf, col0, row0);
-              tma_store_commit();
-            }
-          } else if (row < p.M) {
+            emit_chunk(&tmY, buf, p, row0, tg.row_end, col0, lane, packed);
+          } else if (row < p.M && row < tg.row_end) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (col0 + j < p.N)

@@ -30,6 +30,12 @@ struct GemmArgs {
   float* partials;
   unsigned long long* flags;
   unsigned long long epoch;
+  // Grouped layer (CTA-pair kernel only; group_offsets == nullptr: one
+  // group): rows [offs[g], offs[g+1]) of x and y belong to group g, whose
+  // weight is rows [g N, (g+1) N) of w and whose scales are scale[g N ..].
+  // The offsets are read on the device; values outside [0, M] are clamped.
+  const int* group_offsets;  // device, groups + 1 entries
+  int groups;
 };
 
 // ---- persistent tcgen05 kernel (large M) ---------------------------------

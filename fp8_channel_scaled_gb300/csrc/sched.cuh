@@ -97,4 +97,93 @@ struct WorkIter {
   }
 };
 
+// Where a tile of the work list lies in x, w, y and scale.
+struct TileGeom {
+  int row;      // first x / y row of the 256-row tile
+  int row_end;  // rows >= row_end belong to another group (or lie past M)
+  int wrow;     // first w row of the tile
+  int nb;       // N block: columns [nb BN, nb BN + BN)
+  int sbase;    // offset of the tile's scales in the scale array
+};
+
+// Tile geometry of a (possibly grouped) layer, for tile indices visited in
+// increasing order.  Without groups, tile t is (mb, nb) of the grouped
+// raster over M x N.  With groups, group g owns rows [lo_g, hi_g) with
+// lo_g = max(clamp(offs[g]), hi_{g-1}) and hi_g = max(clamp(offs[g+1]), lo_g)
+// (clamp to [0, M]; hi_{-1} = 0), so groups never overlap whatever the
+// offsets hold; it owns ceil((hi_g - lo_g) / 256) x nnb tiles, numbered after
+// those of groups < g and rastered within the group.  The cursor walks the
+// group offsets forward once.
+struct TileMapper {
+  const int* offs;  // nullptr: one group
+  int groups, M, N, bn, nnb, num_m_blk, group_m;
+  int g, lo, hi, m_blocks;
+  long long before;  // tiles of groups < g
+
+  __device__ TileMapper(const int* offs_, int groups_, int M_, int N_, int bn_, int nnb_,
+                        int num_m_blk_, int group_m_)
+      : offs(offs_), groups(groups_), M(M_), N(N_), bn(bn_), nnb(nnb_), num_m_blk(num_m_blk_),
+        group_m(group_m_), g(0), lo(0), hi(0), m_blocks(0), before(0) {
+    if (offs) load(0, 0);
+  }
+
+  __device__ int clamp_row(int v) const { return v < 0 ? 0 : (v > M ? M : v); }
+
+  // Group gg's rows, given the end of group gg - 1's rows.
+  __device__ void load(int gg, int prev_hi) {
+    g = gg;
+    if (gg >= groups) {
+      lo = hi = M;
+      m_blocks = 0;
+      return;
+    }
+    const int l = clamp_row(__ldg(offs + gg));
+    lo = l < prev_hi ? prev_hi : l;
+    const int h = clamp_row(__ldg(offs + gg + 1));
+    hi = h < lo ? lo : h;
+    m_blocks = (hi - lo + 255) / 256;
+  }
+
+  // Tiles of the whole layer.
+  __device__ long long total() const {
+    if (!offs) return static_cast<long long>(num_m_blk) * nnb;
+    long long t = 0;
+    int prev_hi = 0;
+    for (int gg = 0; gg < groups; ++gg) {
+      int l = clamp_row(__ldg(offs + gg));
+      if (l < prev_hi) l = prev_hi;
+      int h = clamp_row(__ldg(offs + gg + 1));
+      if (h < l) h = l;
+      t += static_cast<long long>((h - l + 255) / 256) * nnb;
+      prev_hi = h;
+    }
+    return t;
+  }
+
+  __device__ TileGeom at(int t) {
+    TileGeom r;
+    int mb, nb;
+    if (!offs) {
+      tile_coords(t, num_m_blk, nnb, group_m, mb, nb);
+      r.row = mb * 256;
+      r.row_end = M;
+      r.wrow = nb * bn;
+      r.nb = nb;
+      r.sbase = 0;
+      return r;
+    }
+    while (g < groups && t >= before + static_cast<long long>(m_blocks) * nnb) {
+      before += static_cast<long long>(m_blocks) * nnb;
+      load(g + 1, hi);
+    }
+    tile_coords(static_cast<int>(t - before), m_blocks > 0 ? m_blocks : 1, nnb, group_m, mb, nb);
+    r.row = lo + mb * 256;
+    r.row_end = hi;
+    r.wrow = g * N + nb * bn;
+    r.nb = nb;
+    r.sbase = g * N;
+    return r;
+  }
+};
+
 }  // namespace fp8g

@@ -222,6 +222,38 @@ int fp8_gemm_scaled_noalloc(const void *x, const void *w, const float *scale, vo
                             int M, int N, int K, fp8gemm_stream_t stream);
 
 /*
+ * fp8_gemm_grouped -- the layer for `groups` independent weight groups (the
+ * experts of a mixture-of-experts layer) in one launch:
+ *
+ *     y[m, n] = bf16_rn( (sum_k x[m, k] * w[g, n, k]) * weight_scale[g, n] )
+ *               for every row m of group g
+ *
+ *   x        device, E4M3 [M, K] row-major: all groups' rows, group g's contiguous
+ *   w        device, E4M3 [groups, N, K] row-major (group g's weight at row g * N)
+ *   scale    device, fp32 [groups, N], 4-byte aligned
+ *   y        device, bf16 [M, N] row-major; rows outside every group are not written
+ *   offsets  device, int32 [groups + 1], 4-byte aligned: group g owns rows
+ *            [offsets[g], offsets[g+1]).  Read by the kernel when it runs, so a
+ *            routing kernel earlier on the stream may write them (no host
+ *            synchronisation).  Values are clamped to [0, M] and made
+ *            non-decreasing (a group starts no earlier than the previous one
+ *            ends), so no two groups share a row whatever the table holds.
+ *   M, N, K  K >= 1; groups * N < 2^31.
+ *
+ * The pages run grouped (MoE up-projection) GEMMs over expert offsets in
+ * bf16 ("Kimi K3 (256k)", "qwen3.8-max" and "claude-fable-5" pages, MoE
+ * up-projection paragraphs); here the CTA-pair kernel walks every group's
+ * 256-row tiles in one persistent work list built from the offsets on the
+ * device.  Operands must be readable by TMA in place: K (or the pitches
+ * fp8gemm_options.ldx / ldw) a multiple of 16 and 16-byte aligned bases, else
+ * FP8GEMM_EALIGN.  Options that select the decode path, one-CTA tiles or the
+ * realigning loader return FP8GEMM_EUNSUPPORTED; tile_n and stages apply.
+ */
+int fp8_gemm_grouped(const void *x, const void *w, const float *scale, void *y,
+                     const int *offsets, int groups, int M, int N, int K,
+                     const fp8gemm_options *opt, fp8gemm_stream_t stream);
+
+/*
  * fp8_gemm_prepare_weight -- copy w [N, K] (row pitch K, any alignment) to
  * w_out with row pitch ldw_out (a multiple of 16, >= K; w_out 16-byte
  * aligned), bytes [K, ldw_out) of each row set to zero.  Passing w_out with

@@ -617,3 +617,80 @@ def test_pitch_arguments_are_checked():
     with pytest.raises(fg.FP8GemmError) as e:  # ldw_out not a multiple of 16
         fg.fp8_gemm_prepare_weight(wd, out)
     assert e.value.status == 2
+
+
+# ------------------------------------------------------------------ grouped (MoE) layer
+def group_ranges(offs, M):
+    """Row ranges the grouped layer assigns: offsets clamped to [0, M] and
+    made non-decreasing (a group starts no earlier than the previous ends)."""
+    clamp = lambda v: min(max(int(v), 0), M)  # noqa: E731
+    ranges, prev_hi = [], 0
+    for g in range(len(offs) - 1):
+        lo = max(clamp(offs[g]), prev_hi)
+        hi = max(clamp(offs[g + 1]), lo)
+        ranges.append((lo, hi))
+        prev_hi = hi
+    return ranges
+
+
+def run_grouped(x, w, s, offs, options=None):
+    M = x.shape[0]
+    G, N, _ = w.shape
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    y.view(torch.int16).fill_(-1)  # sentinel: rows no group owns must keep it
+    od = torch.tensor(np.asarray(offs, np.int32), device="cuda")
+    fg.fp8_gemm_grouped(to_dev(x), to_dev(w), to_dev(s), y, od, options)
+    fg.check_device_error()
+    return y_bits(y)
+
+
+@pytest.mark.parametrize("offs,M", [
+    ([0, 0, 300, 317, 829, 958], 958),        # an empty group, ragged groups
+    ([40, 100, 50, 2000, 20], 300),           # out of order and out of range
+    ([0, 1, 2, 3, 4, 5, 6, 7, 8], 8),         # one row per group
+])
+def test_grouped_layer_matches_per_group_oracle(offs, M):
+    G, N, K = len(offs) - 1, 384, 512
+    x, _, _ = synth.make_inputs(M, 8, K, seed=81)
+    rng = np.random.default_rng(82)
+    w = np.stack([synth.make_inputs(8, N, K, seed=83 + g)[1] for g in range(G)])
+    s = (rng.uniform(0.5, 1.5, (G, N)) / np.sqrt(K)).astype(np.float32)
+    got = run_grouped(x, w, s, offs)
+    covered = np.zeros(M, bool)
+    for g, (lo, hi) in enumerate(group_ranges(offs, M)):
+        if hi > lo:
+            compare(got[lo:hi], oracle.linear(x[lo:hi], w[g], s[g]), f"group {g}")
+            covered[lo:hi] = True
+    assert (got[~covered] == 0xFFFF).all()
+
+
+def test_grouped_layer_equals_separate_calls_on_exact_sums():
+    codes = synth.quantize_e4m3(np.arange(-16, 17, dtype=np.float64))
+    rng = np.random.default_rng(84)
+    counts = [200, 0, 513, 64, 1]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, G, N, K = int(offs[-1]), len(counts), 256, 1024
+    x = rng.choice(codes, (M, K)).astype(np.uint8)
+    w = rng.choice(codes, (G, N, K)).astype(np.uint8)
+    s = (2.0 ** -rng.integers(0, 12, (G, N))).astype(np.float32)
+    got = run_grouped(x, w, s, offs, Options(tile_n=128))
+    for g in range(G):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi > lo:
+            assert np.array_equal(got[lo:hi], oracle.linear(x[lo:hi], w[g], s[g]))
+
+
+def test_grouped_layer_argument_checks():
+    M, G, N, K = 64, 2, 128, 200  # K % 16 != 0: not readable by TMA in place
+    x = to_dev(np.zeros((M, K), np.uint8))
+    w = to_dev(np.zeros((G, N, K), np.uint8))
+    s = to_dev(np.ones((G, N), np.float32))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    od = torch.tensor([0, 32, 64], dtype=torch.int32, device="cuda")
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_grouped(x, w, s, y, od)
+    assert e.value.status == 2
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.fp8_gemm_grouped(x[:, :192], w[:, :, :192].contiguous(), s, y, od,
+                            Options(path=PATH_DECODE))
+    assert e.value.status == 6
