@@ -268,6 +268,39 @@ def bench_workload(key, steps, warmup, device, l2_bytes, stream, fg, prepared_we
     return wl, host, sets, region, per_set
 
 
+def bench_grouped(device, l2_bytes, stream, fg, peak_tf_burst, steps=200, warmup=10):
+    """Context timing of the grouped layer: 8 groups (experts) sharing 8192
+    rows with a seeded skewed split, N = 2048, K = 4096 (the same FLOPs as the
+    square workload); operand sets rotated past 2x L2."""
+    import numpy as np
+    import torch
+    import synth
+    G, M, N, K, seed = 8, 8192, 2048, 4096, 5
+    rng = np.random.default_rng(seed)
+    share = rng.dirichlet(np.full(G, 2.0))
+    counts = np.floor(share * M).astype(np.int64)
+    counts[-1] += M - counts.sum()
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x, _, _ = synth.make_inputs(M, 8, K, seed=seed)
+    w = np.stack([synth.make_inputs(8, N, K, seed=seed + 1 + g)[1] for g in range(G)])
+    s = (rng.uniform(0.5, 1.5, (G, N)) / np.sqrt(K)).astype(np.float32)
+    per_set = x.nbytes + w.nbytes + 2 * M * N
+    n = max(2, math.ceil(2 * l2_bytes / per_set) + 1)
+    xd, wd, sd = (torch.from_numpy(a).to(device) for a in (x, w, s))
+    od = torch.from_numpy(offs).to(device)
+    sets = [(xd.clone(), wd.clone(), sd, torch.empty((M, N), dtype=torch.bfloat16, device=device))
+            for _ in range(n)]
+    call = lambda x_, w_, s_, y_: fg.fp8_gemm_grouped(x_, w_, s_, y_, od, None, stream)  # noqa: E731
+    region = time_steps(sets, steps, warmup, stream, call)
+    fg.check_device_error(stream)
+    t = region / steps
+    tf = 2.0 * M * N * K / t / 1e12
+    return {"workload": f"grouped {G} groups, rows {counts.tolist()}, N={N}, K={K}",
+            "us_per_call": round(t * 1e6, 2), "TFLOP/s": round(tf, 1),
+            "frac_fp8_measured_burst": round(tf / peak_tf_burst, 4), "launches": 1,
+            "l2": f"rotating {n} sets"}
+
+
 # ---------------------------------------------------------------- arms
 def run_ours(args):
     import torch
@@ -444,6 +477,7 @@ def run_ours(args):
                            "l2": "no rotation (launch-bound)" if key2 == "small" else f"rotating {len(sets2)} sets"}
             del sets2
             torch.cuda.empty_cache()
+        others["grouped_moe"] = bench_grouped(device, l2, stream, fg, peak_tf_burst)
         line["workloads"] = others
 
     # ---- CPU baseline (oracle on host cores, bounded sample) and a parity check of that sample
