@@ -161,10 +161,15 @@ __global__ void __launch_bounds__(kThreads)
       const int ptid = static_cast<int>(threadIdx.x);
       uint32_t stage = 0, phase = 0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
+        // all of this K block's loads (w rows and x rows) are issued before
+        // the first is used, so the block costs one memory latency
+        RealignRegs<kBN, 128> ga;
+        RealignRegs<MP, 128> gb;
+        realign_load(ga, p.w, p.N, p.K, n0, kb * kBK, ptid);
+        realign_load(gb, p.x, p.M, p.K, 0, kb * kBK, ptid);
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) break;
-        load_tile_realign<kBN, 128, 4>(sA(stage), p.w, p.N, p.K, n0, kb * kBK, ptid);
-        load_tile_realign<MP, 128, (MP * 8 / 128) >= 4 ? 4 : (MP * 8 / 128)>(
-            sB(stage), p.x, p.M, p.K, 0, kb * kBK, ptid);
+        realign_store(sA(stage), ga, ptid);
+        realign_store(sB(stage), gb, ptid);
         fence_proxy_async_smem();
         mbar_arrive(full_bar(stage));
         if (++stage == STAGES) {

@@ -103,4 +103,65 @@ __device__ __forceinline__ void load_tile_realign(uint32_t dst, const uint8_t* _
   }
 }
 
+// The same copy split into a load half and a store half, so that a producer
+// can issue the loads of the next K block before it stores this one (one
+// memory latency per K block instead of one per batch of chunks, with the
+// next block's loads already in flight).  Thread tid holds chunks
+// u = i * NT + tid (i < PER): row u / 8, 16-byte chunk u % 8; since NT is a
+// multiple of 8, lanes 8j .. 8j + 7 of a warp hold one row's 8 chunks in
+// order, so the second source word of a chunk is the next lane's first word
+// (taken by shuffle) except for a row's last chunk, which loads it.  A lane
+// loads a word only if it holds a byte of the row: word start < row + K.
+template <int R, int NT>
+struct RealignRegs {
+  static constexpr int PER = R * 8 / NT;
+  static_assert((R * 8) % NT == 0 && NT % 32 == 0, "units must split evenly over warps");
+  uint4 lo[PER];
+  uint4 tail[PER];   // a row's last chunk: the word after it
+  uint32_t sh[PER];
+  int valid[PER];    // bytes of the chunk that are < K (<= 0: none)
+};
+
+template <int R, int NT>
+__device__ __forceinline__ void realign_load(RealignRegs<R, NT>& g, const uint8_t* __restrict__ src,
+                                             int rows_total, int K, int r0, int k0, int tid) {
+#pragma unroll
+  for (int i = 0; i < RealignRegs<R, NT>::PER; ++i) {
+    const int u = i * NT + tid;
+    const int r = u >> 3, c = u & 7;
+    const int grow = r0 + r, kc = k0 + 16 * c;
+    g.lo[i] = make_uint4(0, 0, 0, 0);
+    g.tail[i] = make_uint4(0, 0, 0, 0);
+    g.sh[i] = 0;
+    g.valid[i] = 0;
+    if (grow < rows_total) {
+      const uint8_t* row = src + static_cast<size_t>(grow) * static_cast<size_t>(K);
+      const uint32_t sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row + kc) & 15u);
+      const uint8_t* base = row + kc - sh;  // aligned word holding byte kc
+      g.sh[i] = sh;
+      g.valid[i] = K - kc;
+      // word [base, base + 16) holds row bytes iff base < row + K
+      if (kc - static_cast<int>(sh) < K) g.lo[i] = ldg_nc_v4(base);
+      if (c == 7 && sh != 0u && kc + 16 - static_cast<int>(sh) < K) g.tail[i] = ldg_nc_v4(base + 16);
+    }
+  }
+}
+
+template <int R, int NT>
+__device__ __forceinline__ void realign_store(uint32_t dst, const RealignRegs<R, NT>& g, int tid) {
+#pragma unroll
+  for (int i = 0; i < RealignRegs<R, NT>::PER; ++i) {
+    const int u = i * NT + tid;
+    const int r = u >> 3, c = u & 7;
+    uint4 hi;
+    hi.x = __shfl_down_sync(0xffffffffu, g.lo[i].x, 1);
+    hi.y = __shfl_down_sync(0xffffffffu, g.lo[i].y, 1);
+    hi.z = __shfl_down_sync(0xffffffffu, g.lo[i].z, 1);
+    hi.w = __shfl_down_sync(0xffffffffu, g.lo[i].w, 1);
+    if (c == 7) hi = g.tail[i];
+    const uint4 v = keep_bytes(realign16(g.lo[i], hi, g.sh[i]), g.valid[i]);
+    sts_v4(dst + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)), v);
+  }
+}
+
 }  // namespace fp8g

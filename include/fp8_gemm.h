@@ -143,10 +143,10 @@ typedef struct {
  *   M,N,K  >= 0.  M == 0 or N == 0: nothing is launched.  K == 0: y = 0.
  *
  * Rows whose pitch K is not a multiple of 16 bytes (e.g. K = 4127), or
- * operands not 16-byte aligned, cannot be tiled by TMA.  On the main path
- * they are first copied by a repitch kernel into a workspace with a
- * 16-byte pitch and zero pad bytes (two launches); on the decode path, or
- * with no_workspace, an in-kernel realigning producer loads them directly.
+ * operands not 16-byte aligned, cannot be tiled by TMA.  They are first
+ * copied by a repitch kernel into a workspace with a 16-byte pitch and zero
+ * pad bytes (two launches); with no_workspace (or when no workspace memory
+ * can be had) an in-kernel realigning producer loads them directly.
  * Either way bytes past K count as zeros, which adds exactly nothing (the
  * zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
  * paragraph).  Nothing is cached between calls.
