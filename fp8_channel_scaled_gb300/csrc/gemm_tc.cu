@@ -171,13 +171,21 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, REALIGN>::kThreads, 1)
         int mb, nb;
         tile_coords(t, num_m_blk, num_n_blk, group_m, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
+          // x rows in one load round (issued before waiting for the stage),
+          // then w rows in two rounds of BN / 2 rows
+          RealignRegs<kBM, 128> ga;
+          realign_load(ga, p.x, p.M, p.K, mb * kBM, kb * kBK, ptid);
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, wc, kErrWaitProducer)) {
             ok = false;
             break;
           }
-          load_tile_realign<kBM, 128, 4>(sA(stage), p.x, p.M, p.K, mb * kBM, kb * kBK, ptid);
-          load_tile_realign<BN, 128, ((BN * 8 / 128) % 4 == 0) ? 4 : 2>(sB(stage), p.w, p.N, p.K,
-                                                                       nb * BN, kb * kBK, ptid);
+          realign_store(sA(stage), ga, ptid);
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            RealignRegs<BN / 2, 128> gb;
+            realign_load(gb, p.w, p.N, p.K, nb * BN + h * (BN / 2), kb * kBK, ptid);
+            realign_store(sB(stage) + static_cast<uint32_t>(h * (BN / 2) * 128), gb, ptid);
+          }
           fence_proxy_async_smem();
           mbar_arrive(full_bar(stage));
           if (++stage == STAGES) {

@@ -58,60 +58,20 @@ __device__ __forceinline__ uint4 keep_bytes(uint4 v, int valid) {
 
 // Copy rows [r0, r0+R) x bytes [k0, k0+128) of a row-major byte matrix with
 // `rows_total` rows and pitch K bytes into the K-major 128-byte-swizzled
-// tile at shared address `dst` (1024-byte aligned): row r's 16-byte chunk c
-// lands at r*128 + ((c ^ (r & 7)) * 16).  Rows >= rows_total and bytes at
-// k >= K are written as zeros.  NT threads (tid in [0, NT)) share the work;
-// consecutive threads take consecutive chunks of a row, so loads coalesce.
-template <int R, int NT, int BATCH>
-__device__ __forceinline__ void load_tile_realign(uint32_t dst, const uint8_t* __restrict__ src,
-                                                  int rows_total, int K, int r0, int k0,
-                                                  int tid) {
-  constexpr int UNITS = R * 8;
-  static_assert(UNITS % NT == 0, "units must split evenly");
-  constexpr int PER = UNITS / NT;
-  static_assert(PER % BATCH == 0, "batch must divide the per-thread units");
-#pragma unroll
-  for (int b = 0; b < PER; b += BATCH) {
-    uint4 lo[BATCH], hi[BATCH];
-    uint32_t sh[BATCH];
-    int valid[BATCH];
-#pragma unroll
-    for (int i = 0; i < BATCH; ++i) {
-      const int u = (b + i) * NT + tid;
-      const int r = u >> 3, c = u & 7;
-      const int grow = r0 + r, kc = k0 + 16 * c;
-      lo[i] = make_uint4(0, 0, 0, 0);
-      hi[i] = make_uint4(0, 0, 0, 0);
-      sh[i] = 0;
-      valid[i] = 0;
-      if (grow < rows_total && kc < K) {
-        valid[i] = min(16, K - kc);
-        const uint8_t* p = src + static_cast<size_t>(grow) * static_cast<size_t>(K) + kc;
-        sh[i] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p) & 15u);
-        const uint8_t* base = p - sh[i];
-        lo[i] = ldg_nc_v4(base);
-        if (sh[i] != 0u && valid[i] > 16 - static_cast<int>(sh[i])) hi[i] = ldg_nc_v4(base + 16);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < BATCH; ++i) {
-      const int u = (b + i) * NT + tid;
-      const int r = u >> 3, c = u & 7;
-      uint4 v = keep_bytes(realign16(lo[i], hi[i], sh[i]), valid[i]);
-      sts_v4(dst + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)), v);
-    }
-  }
-}
-
-// The same copy split into a load half and a store half, so that a producer
-// can issue the loads of the next K block before it stores this one (one
-// memory latency per K block instead of one per batch of chunks, with the
-// next block's loads already in flight).  Thread tid holds chunks
-// u = i * NT + tid (i < PER): row u / 8, 16-byte chunk u % 8; since NT is a
-// multiple of 8, lanes 8j .. 8j + 7 of a warp hold one row's 8 chunks in
-// order, so the second source word of a chunk is the next lane's first word
-// (taken by shuffle) except for a row's last chunk, which loads it.  A lane
-// loads a word only if it holds a byte of the row: word start < row + K.
+// shared-memory layout of one operand stage (row r, 16-byte chunk c at
+// r * 128 + ((c ^ (r & 7)) << 4)), zero past rows_total and past K.  It is
+// split into a load half and a store half, so that a producer issues all
+// of a block's loads (even before it waits for the stage to be free) and
+// then stores them: one memory latency per block, not one per batch of
+// chunks.  The loads sit in registers, so a producer cannot keep enough in
+// flight to stream at HBM rate; callers repitch instead when they can.
+//
+// Thread tid holds chunks u = i * NT + tid (i < PER): row u / 8, 16-byte
+// chunk u % 8.  Since NT is a multiple of 8, lanes 8j .. 8j + 7 of a warp
+// hold one row's 8 chunks in order, so the second source word of a chunk is
+// the next lane's first word (taken by shuffle) except for a row's last
+// chunk, which loads it.  A lane loads a word only if it holds a byte of the
+// row: word start < row + K.
 template <int R, int NT>
 struct RealignRegs {
   static constexpr int PER = R * 8 / NT;
