@@ -34,6 +34,7 @@ constexpr int kBK = 128;   // bytes of K per stage
 constexpr int kMmaK = 32;
 constexpr int kMmaWarp = 4;
 constexpr int kThreads = 160;
+constexpr int kMaxSplits = 8;  // largest cluster the planner forms
 
 template <int MP>
 __host__ __device__ constexpr int tmem_cols_for() {
@@ -58,7 +59,9 @@ struct DCfg {
   static constexpr int kBarOff = kDataBytes;
   // full[S], empty[S], acc_full, mma_done, then tmem holder + abort flag
   static constexpr int kNumBars = 2 * STAGES + 2;
-  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  // the n-tile's 128 scales, staged for the reduction
+  static constexpr int kScaleOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
+  static constexpr int kSmemBytes = 1024 + kScaleOff + kBN * 4;
   static constexpr int kTmemCols = tmem_cols_for<MP>();
   static_assert(MP % 32 == 0 && MP >= 32 && MP <= 128, "MP");
 };
@@ -87,6 +90,7 @@ __global__ void __launch_bounds__(kThreads)
   auto sA = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes); };
   auto sB = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes + C::kABytes); };
   const uint32_t part = sbase;  // fp32 partials [MP][128], reuses the ring after the mainloop
+  float* scale_s = reinterpret_cast<float*>(gbase + C::kScaleOff);
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -182,10 +186,15 @@ __global__ void __launch_bounds__(kThreads)
     // ------------------------------------------------------------ partials
     // TMEM lane = n within the tile, column = m.  Park them in shared memory
     // as part[m][n] so the cluster reduction reads 16-byte runs along n.
+    // The scale of column n is fetched now, its latency hidden behind the
+    // last MMAs, and staged in shared memory for the reduction.
+    const uint32_t n_local = warp * 32u + lane;
+    const float my_scale =
+        n0 + static_cast<int>(n_local) < p.N ? __ldg(p.scale + n0 + n_local) : 0.f;
     const bool have_acc = (my_kb == 0) || mbar_wait_bounded(acc_full_bar, 0u, wc, kErrWaitEpilogue);
+    scale_s[n_local] = my_scale;
     if (have_acc) {
       tc_fence_after_sync();
-      const uint32_t n_local = warp * 32u + lane;
 #pragma unroll 1
       for (int c = 0; c < MP / 32; ++c) {
         uint32_t v[32];
@@ -238,50 +247,61 @@ __global__ void __launch_bounds__(kThreads)
   // ---------------------------------------------------------------- reduce
   // Every CTA of the cluster has parked its partials; each now reduces an
   // equal share of the M x 128 outputs of this n-tile, reading all partials
-  // through distributed shared memory, and stores scaled bf16.
+  // through distributed shared memory, and stores scaled bf16.  A thread
+  // takes two float4 groups at a time and issues all their remote loads
+  // before it sums any, so each round pays one remote latency.
   tc_fence_before_sync();
   cluster_sync_all();
   {
     const int groups = p.M * (kBN / 4);  // float4 groups of valid rows
     const int g_begin = static_cast<int>((static_cast<long long>(groups) * rank) / splits);
     const int g_end = static_cast<int>((static_cast<long long>(groups) * (rank + 1)) / splits);
-    for (int g = g_begin + static_cast<int>(threadIdx.x); g < g_end; g += kThreads) {
+    auto finish = [&](int g, const float4* v) {
+      float4 s = v[0];  // summed in split order
+#pragma unroll
+      for (int q = 1; q < kMaxSplits; ++q) {
+        if (q < splits) {
+          s.x += v[q].x;
+          s.y += v[q].y;
+          s.z += v[q].z;
+          s.w += v[q].w;
+        }
+      }
       const int m = g / (kBN / 4);
       const int nl = (g % (kBN / 4)) * 4;
-      const uint32_t off = part + static_cast<uint32_t>((m * kBN + nl) * 4);
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < splits; ++q) {
-        const float4 v = ld_dsmem_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
-      }
+      const float4 sc = *reinterpret_cast<const float4*>(scale_s + nl);
       const int n = n0 + nl;
       uint16_t* yr = p.y + static_cast<size_t>(m) * static_cast<size_t>(p.N);
-      if (n + 4 <= p.N) {
-        const float4 sc = make_float4(__ldg(p.scale + n), __ldg(p.scale + n + 1),
-                                      __ldg(p.scale + n + 2), __ldg(p.scale + n + 3));
-        const uint32_t lo = pack_bf16x2(s.x * sc.x, s.y * sc.y);
-        const uint32_t hi = pack_bf16x2(s.z * sc.z, s.w * sc.w);
-        if (p.vec_store) {
-          *reinterpret_cast<uint2*>(yr + n) = make_uint2(lo, hi);
-        } else {
-          yr[n] = static_cast<uint16_t>(lo & 0xFFFFu);
-          yr[n + 1] = static_cast<uint16_t>(lo >> 16);
-          yr[n + 2] = static_cast<uint16_t>(hi & 0xFFFFu);
-          yr[n + 3] = static_cast<uint16_t>(hi >> 16);
-        }
+      const uint32_t lo = pack_bf16x2(s.x * sc.x, s.y * sc.y);
+      const uint32_t hi = pack_bf16x2(s.z * sc.z, s.w * sc.w);
+      if (n + 4 <= p.N && p.vec_store) {
+        *reinterpret_cast<uint2*>(yr + n) = make_uint2(lo, hi);
       } else {
-        const float sv[4] = {s.x, s.y, s.z, s.w};
+        const uint16_t h[4] = {static_cast<uint16_t>(lo & 0xFFFFu), static_cast<uint16_t>(lo >> 16),
+                               static_cast<uint16_t>(hi & 0xFFFFu), static_cast<uint16_t>(hi >> 16)};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (n + j < p.N) {
-            const uint32_t b = pack_bf16x2(sv[j] * __ldg(p.scale + n + j), 0.f);
-            yr[n + j] = static_cast<uint16_t>(b & 0xFFFFu);
-          }
+        for (int j = 0; j < 4; ++j)
+          if (n + j < p.N) yr[n + j] = h[j];
+      }
+    };
+    auto group_off = [&](int g) {
+      return part + static_cast<uint32_t>(((g / (kBN / 4)) * kBN + (g % (kBN / 4)) * 4) * 4);
+    };
+    for (int g0 = g_begin + static_cast<int>(threadIdx.x); g0 < g_end; g0 += 2 * kThreads) {
+      const int g1 = g0 + kThreads;
+      const bool two = g1 < g_end;
+      const uint32_t off0 = group_off(g0);
+      const uint32_t off1 = two ? group_off(g1) : off0;
+      float4 v0[kMaxSplits], v1[kMaxSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxSplits; ++q) {
+        if (q < splits) {
+          v0[q] = ld_dsmem_f32x4(mapa_shared(off0, static_cast<uint32_t>(q)));
+          v1[q] = ld_dsmem_f32x4(mapa_shared(off1, static_cast<uint32_t>(q)));
         }
       }
+      finish(g0, v0);
+      if (two) finish(g1, v1);
     }
   }
   // nobody leaves while another CTA may still read its shared memory
