@@ -10,9 +10,11 @@
 // padding only to the next multiple of 16 bytes.  Zero bytes add exactly
 // nothing to a dot product, so results equal the unpadded ones.
 //
-// One warp copies a segment of 64 output chunks (1 KiB) of one row of the
-// stacked [x; w] matrix, so that even a copy of a few thousand rows has tens
-// of thousands of loads in flight at once.  Output chunk j of a row (bytes
+// One warp copies a segment of 64, 96 or 128 output chunks (the width that
+// leaves the fewest lanes idle at the row's end: 96 for K = 4127) of one row
+// of the stacked [x; w] matrix, issuing all its loads before using any, so
+// that even a copy of a few thousand rows has tens of thousands of loads in
+// flight at once.  Output chunk j of a row (bytes
 // [16 j, 16 j + 16)) is bytes [sh, sh + 16) of the two aligned 16-byte source
 // words at abase + 16 j and abase + 16 (j + 1), where abase is the row start
 // rounded down to 16 bytes and sh the remainder: lane l loads the first word
@@ -29,11 +31,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kU = 2;                // output chunks per lane
-constexpr int kSegChunks = 32 * kU;  // output chunks per warp
 
+// kU output chunks per lane, 32 kU per warp (one row segment).
+template <int kU>
 __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a,
                                                            const int segs_per_row) {
+  constexpr int kSegChunks = 32 * kU;
   griddep_launch_dependents();
   griddep_wait();
   const uint32_t lane = threadIdx.x & 31u;
@@ -50,11 +53,15 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a,
   const long long span = static_cast<long long>(sh) + a.K;  // bytes from abase to the row's end
   const int cpr = a.Kp / 16;                               // output chunks per row
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 lo[kU];
+  // every load of the segment is issued before any is used: the words of
+  // the lanes' own chunks, and lane 31's word past each 32-chunk run
+  uint4 lo[kU], tail[kU];
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
     const long long off = 16LL * (j0 + u * 32 + static_cast<int>(lane));
     lo[u] = off < span ? ldg_nc_v4(abase + off) : zero;
+    tail[u] = zero;
+    if (lane == 31u && sh != 0u && off + 16 < span) tail[u] = ldg_nc_v4(abase + off + 16);
   }
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
@@ -64,10 +71,7 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a,
     hi.y = __shfl_down_sync(0xffffffffu, lo[u].y, 1);
     hi.z = __shfl_down_sync(0xffffffffu, lo[u].z, 1);
     hi.w = __shfl_down_sync(0xffffffffu, lo[u].w, 1);
-    if (lane == 31u) {
-      const long long off = 16LL * (j + 1);
-      hi = (sh != 0u && off < span) ? ldg_nc_v4(abase + off) : zero;
-    }
+    if (lane == 31u) hi = tail[u];
     if (j < cpr) {
       const uint4 v = keep_bytes(realign16(lo[u], hi, sh), a.K - 16 * j);
       *reinterpret_cast<uint4*>(dst + 16LL * j) = v;
@@ -80,7 +84,17 @@ __global__ void __launch_bounds__(kThreads) repitch_kernel(const RepitchArgs a,
 cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   const long long rows = a.rows_x + a.rows_w;
   if (rows <= 0 || a.Kp <= 0) return cudaSuccess;
-  const int segs = (a.Kp / 16 + kSegChunks - 1) / kSegChunks;
+  // segment width: the fewest idle lane slots over a row (ties: wider)
+  const int cpr = a.Kp / 16;
+  int best_u = 2, best_slots = 0;
+  for (int u = 2; u <= 4; ++u) {
+    const int slots = (cpr + 32 * u - 1) / (32 * u) * (32 * u);
+    if (best_slots == 0 || slots <= best_slots) {
+      best_u = u;
+      best_slots = slots;
+    }
+  }
+  const int segs = (cpr + 32 * best_u - 1) / (32 * best_u);
   const long long blocks = (rows * segs + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -91,7 +105,11 @@ cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   set_pdl(attr[0]);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, repitch_kernel, a, segs);
+  switch (best_u) {
+    case 2: return cudaLaunchKernelEx(&cfg, repitch_kernel<2>, a, segs);
+    case 3: return cudaLaunchKernelEx(&cfg, repitch_kernel<3>, a, segs);
+    default: return cudaLaunchKernelEx(&cfg, repitch_kernel<4>, a, segs);
+  }
 }
 
 }  // namespace fp8g
