@@ -142,8 +142,12 @@ def _status_string(status: int) -> str:
 
 
 def _stream_handle(stream) -> int:
+    """Raw cudaStream_t of `stream` (None: the current device's current stream)."""
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:  # same value as current_stream().cuda_stream, without the object
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -151,7 +155,10 @@ def _stream_handle(stream) -> int:
 
 
 def _ptr(t) -> int:
-    return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+    try:
+        return t.data_ptr()
+    except AttributeError:
+        return int(t)
 
 
 def _row_pitch(t, name):
@@ -164,22 +171,29 @@ def _row_pitch(t, name):
 
 
 def _shapes(x, w, scale, y, strided=False):
-    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
-        raise ValueError(f"x {tuple(x.shape)} and w {tuple(w.shape)} must be [M,K] and [N,K]")
-    M, K = x.shape
-    N = w.shape[0]
-    if tuple(scale.shape) != (N,) or tuple(y.shape) != (M, N):
-        raise ValueError(f"scale {tuple(scale.shape)} / y {tuple(y.shape)} do not match M={M} N={N}")
-    for name, t in (("x", x), ("w", w), ("scale", scale), ("y", y)):
-        if strided and name in ("x", "w"):
-            _row_pitch(t, name)
-        elif not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+    xs, ws, ss, ys = x.shape, w.shape, scale.shape, y.shape
+    if len(xs) != 2 or len(ws) != 2 or xs[1] != ws[1]:
+        raise ValueError(f"x {tuple(xs)} and w {tuple(ws)} must be [M,K] and [N,K]")
+    M, K = xs
+    N = ws[0]
+    if len(ss) != 1 or ss[0] != N or len(ys) != 2 or ys[0] != M or ys[1] != N:
+        raise ValueError(f"scale {tuple(ss)} / y {tuple(ys)} do not match M={M} N={N}")
+    if strided:
+        if not x.is_contiguous():
+            _row_pitch(x, "x")
+        if not w.is_contiguous():
+            _row_pitch(w, "w")
+    elif not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError(("x" if not x.is_contiguous() else "w") + " must be contiguous")
+    if not scale.is_contiguous():
+        raise ValueError("scale must be contiguous")
+    if not y.is_contiguous():
+        raise ValueError("y must be contiguous")
     if x.element_size() != 1 or w.element_size() != 1:
         raise TypeError("x and w must be 1-byte E4M3 tensors (uint8 or float8_e4m3fn)")
     if scale.element_size() != 4 or y.element_size() != 2:
         raise TypeError("scale must be float32 and y bfloat16")
-    return int(M), int(N), int(K)
+    return M, N, K
 
 
 def _check(status: int, what: str):
@@ -199,13 +213,14 @@ def fp8_gemm_scaled_ex(x, w, scale, y, options: Options | None = None, stream=No
     """As fp8_gemm_scaled with options; x and w may be row-major views with a
     row pitch (e.g. buf[:, :K]): their pitches go to options.ldx / ldw."""
     M, N, K = _shapes(x, w, scale, y, strided=True)
-    o = (options or Options())._c()
+    o = options._c() if options is not None else _COptions()  # all-zero: the defaults
     if not o.ldx and _row_pitch(x, "x") != K:
         o.ldx = _row_pitch(x, "x")
     if not o.ldw and _row_pitch(w, "w") != K:
         o.ldw = _row_pitch(w, "w")
     _check(lib().fp8_gemm_scaled_ex(_ptr(x), _ptr(w), _ptr(scale), _ptr(y), M, N, K,
-                                    ctypes.byref(o), _stream_handle(stream)), "fp8_gemm_scaled_ex")
+                                    ctypes.byref(o), _stream_handle(stream)),
+           "fp8_gemm_scaled_ex")
 
 
 def fp8_gemm_scaled_noalloc(x, w, scale, y, stream=None) -> None:
