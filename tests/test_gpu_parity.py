@@ -281,6 +281,47 @@ def test_decode_realign(M):
     check_full(x, w, s, Options(path=PATH_DECODE, force_realign=True), what=f"decode realign M={M}")
 
 
+# ------------------------------------------------------------------ seeded random sweep
+def _random_cases(n=28, seed=20261202):
+    """Shapes and plan options drawn once from a fixed seed: sizes with
+    every residue against the tile widths, the 16-byte K pitch and the
+    128-byte K block, on every path and tile kind the planner can pick."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for i in range(n):
+        M = int(rng.integers(1, 700))
+        N = int(rng.integers(1, 1300))
+        K = int(rng.integers(1, 2200))
+        kind = i % 7
+        if kind == 0:
+            opts = None
+        elif kind == 1:
+            opts = dict(path=PATH_MAIN, mma_ctas=1, tile_n=int(rng.choice([128, 160, 192, 224, 256])))
+        elif kind == 2:
+            opts = dict(path=PATH_MAIN, mma_ctas=2, tile_n=int(rng.choice([128, 160, 192, 224, 256])))
+        elif kind == 3:
+            opts = dict(path=PATH_MAIN, mma_ctas=2, split_tail=True)
+        elif kind == 4:
+            M = int(rng.integers(1, 129))
+            opts = dict(path=PATH_DECODE, splits=int(rng.integers(1, 9)))
+        elif kind == 5:
+            opts = dict(path=PATH_MAIN, no_workspace=True)
+        else:
+            M = int(rng.integers(1, 129))
+            opts = dict(path=PATH_DECODE)
+        cases.append((M, N, K, opts, int(rng.integers(0, 2 ** 31))))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,opts,seed", _random_cases())
+def test_random_shapes_and_options(M, N, K, opts, seed):
+    x, w, s = synth.make_inputs(M, N, K, seed=seed)
+    o = None if opts is None else Options(**opts)
+    if o is not None and o.path == PATH_DECODE and o.splits > max(1, (K + 127) // 128):
+        o.splits = 0  # more splits than K blocks: let the planner choose
+    check_full(x, w, s, o, what=f"random {M}x{N}x{K} {opts}")
+
+
 # ------------------------------------------------------------------ bitwise pins
 @pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
 def test_one_hot_weights_reproduce_x_bitwise(path):
