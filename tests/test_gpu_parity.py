@@ -322,6 +322,52 @@ def test_random_shapes_and_options(M, N, K, opts, seed):
     check_full(x, w, s, o, what=f"random {M}x{N}x{K} {opts}")
 
 
+# ------------------------------------------------------------------ concurrent host threads
+def test_concurrent_host_threads_on_separate_streams():
+    # The binding releases the GIL inside each C call, so these threads enter
+    # the library at the same time: plan caches, the workspace pool (the
+    # K = 4127 shape repitches into it) and the split tail's epochs are shared.
+    import threading
+    cases = [
+        (96, 640, 4127, None), (256, 512, 1024, None), (32, 1024, 512, Options(path=PATH_DECODE)),
+        (300, 520, 640, Options(path=PATH_MAIN, mma_ctas=2, split_tail=True)),
+    ]
+    data = []
+    for i, (M, N, K, o) in enumerate(cases):
+        x, w, s = synth.make_inputs(M, N, K, seed=900 + i)
+        data.append((to_dev(x), to_dev(w), to_dev(s), o, oracle.linear(x, w, s)))
+    outs = [[None] * 6 for _ in cases]
+    errors = []
+
+    def worker(i):
+        try:
+            xd, wd, sd, o, _ = data[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for r in range(6):
+                    y = torch.empty((xd.shape[0], wd.shape[0]), dtype=torch.bfloat16, device="cuda")
+                    if o is None:
+                        fg.fp8_gemm_scaled(xd, wd, sd, y, st)
+                    else:
+                        fg.fp8_gemm_scaled_ex(xd, wd, sd, y, o, st)
+                    outs[i][r] = y
+            st.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    fg.check_device_error()
+    for i, (_, _, _, _, ref) in enumerate(data):
+        for r in range(6):
+            compare(y_bits(outs[i][r]), ref, f"thread {i} call {r}")
+
+
 # ------------------------------------------------------------------ bitwise pins
 @pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
 def test_one_hot_weights_reproduce_x_bitwise(path):
