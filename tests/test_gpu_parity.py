@@ -322,6 +322,39 @@ def test_random_shapes_and_options(M, N, K, opts, seed):
     check_full(x, w, s, o, what=f"random {M}x{N}x{K} {opts}")
 
 
+# ------------------------------------------------------------------ maximum sizes
+@pytest.mark.parametrize("N,ctas", [(16384, 2), (16384, 1), (16383, 2)])
+def test_output_larger_than_2gib(N, ctas):
+    # y holds more than 2^31 bytes, so every store path (TMA store, 16-byte
+    # stores of one-CTA tiles, element stores when N % 8 != 0) must index it
+    # with 64-bit offsets; rows around byte offset 2^31 and the last rows are
+    # checked against the oracle.
+    M, K = 70000, 32
+    assert M * N * 2 > 2 ** 31
+    x, w, s = synth.make_inputs(M, N, K, seed=77)
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_scaled_ex(xd, wd, sd, y, Options(path=PATH_MAIN, mma_ctas=ctas))
+    fg.check_device_error()
+    edge = (2 ** 31) // (2 * N)
+    rng = np.random.default_rng(78)
+    rows = np.unique(np.concatenate([[0, edge - 1, edge, edge + 1, M - 2, M - 1],
+                                     rng.integers(0, M, 10)]))
+    got = y_bits(y[torch.from_numpy(rows).cuda()])
+    compare(got, oracle.linear_rows(x, w, s, rows), f"y > 2 GiB N={N} ctas={ctas}")
+    del y
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M,N,path", [(256, 384, PATH_MAIN), (32, 512, PATH_DECODE)])
+def test_long_k(M, N, path):
+    # 40,000-byte rows: hundreds of K blocks, so every ring barrier wraps its
+    # phase many times within one tile
+    K = 40000
+    x, w, s = synth.make_inputs(M, N, K, seed=79)
+    check_full(x, w, s, Options(path=path), what=f"long K {M}x{N}x{K}")
+
+
 # ------------------------------------------------------------------ concurrent host threads
 def test_concurrent_host_threads_on_separate_streams():
     # The binding releases the GIL inside each C call, so these threads enter
