@@ -58,7 +58,7 @@ struct DevState {
   void* noalloc_ws = nullptr;    // device address of g_noalloc_workspace on this device
   // Occupancy of each kernel configuration, queried once on first use so that
   // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
-  int tc2_pairs[5][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
+  int tc2_pairs[6][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
   int dec_blocks[3][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
   int dec_clusters[3][6][2][9];  // ... [splits]: resident clusters
   std::atomic<unsigned long long> calls{0};  // split-tail calls launched (epoch source)
@@ -87,8 +87,8 @@ unsigned long long budget_ns() {
   return g_budget_ns;
 }
 
-const int kTcTiles[] = {256, 224, 192, 160, 128};
-const int kTcStages[] = {3, 4, 5, 6, 7};
+const int kTcTiles[] = {256, 224, 192, 160, 128, 64};  // 64: one-CTA tiles only
+const int kTcStages[] = {3, 4, 5, 6, 7, 8, 9};
 const int kTc2Stages[] = {3, 4};
 const int kDecMp[] = {32, 64, 128};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};

@@ -316,12 +316,15 @@ Entry make_entry() {
 
 // N tiles and pipeline depths that are built: for each N tile the deepest
 // ring that fits in shared memory (and one shallower ring), plus the
-// realigning-producer variants used when no workspace can be had.
+// realigning-producer variants used when no workspace can be had.  64-wide
+// tiles serve 129-256 rows with few N blocks: twice the CTAs of 128-wide
+// tiles stream the weight (256 x 4096 x 4096: 13.3 us against 14.2 us).
 const Entry kEntries[] = {
     make_entry<256, 4, false>(), make_entry<256, 3, false>(), make_entry<224, 5, false>(),
     make_entry<224, 4, false>(), make_entry<192, 5, false>(), make_entry<160, 6, false>(),
-    make_entry<128, 7, false>(), make_entry<128, 6, false>(), make_entry<256, 4, true>(),
-    make_entry<224, 4, true>(),  make_entry<128, 6, true>(),
+    make_entry<128, 7, false>(), make_entry<128, 6, false>(), make_entry<64, 9, false>(),
+    make_entry<64, 8, false>(),  make_entry<256, 4, true>(),  make_entry<224, 4, true>(),
+    make_entry<128, 6, true>(),
 };
 
 const Entry* find(int bn, int stages, bool realign) {

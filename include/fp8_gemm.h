@@ -84,7 +84,8 @@ typedef struct {
     int path;           /* FP8GEMM_PATH_* */
     int force_realign;  /* 1: load operands with the in-kernel realigning
                            producer even when TMA could (tests that loader) */
-    int tile_n;         /* main path N tile: 0 auto, or 128, 160, 192, 224, 256 */
+    int tile_n;         /* main path N tile: 0 auto, or 128, 160, 192, 224, 256;
+                           64 with one-CTA tiles only */
     int stages;         /* pipeline depth: 0 auto */
     int splits;         /* decode path K splits (cluster size): 0 auto, 1..8 */
     int no_workspace;   /* 1: never repitch; rows TMA cannot tile are then

@@ -77,10 +77,21 @@ def test_main_path_shapes(M, N, K, ctas):
     check_full(x, w, s, Options(path=PATH_MAIN, mma_ctas=ctas), what=f"main {M}x{N}x{K} ctas={ctas}")
 
 
-@pytest.mark.parametrize("bn", [128, 160, 192, 224, 256])
+@pytest.mark.parametrize("bn", [64, 128, 160, 192, 224, 256])
 def test_main_path_tiles(bn):
     x, w, s = synth.make_inputs(300, 520, 640, seed=5)
     check_full(x, w, s, Options(path=PATH_MAIN, tile_n=bn, mma_ctas=1), what=f"main bn={bn}")
+
+
+def test_narrow_tiles_for_mid_m():
+    # 129-256 rows with few N blocks: 64-wide one-CTA tiles (twice the CTAs of
+    # 128-wide ones); the CTA-pair kernel has no 64-wide tile
+    p = fg.plan(256, 4096, 4096)
+    assert (p.path, p.tile_m, p.tile_n, p.cluster) == (PATH_MAIN, 128, 64, 1)
+    with pytest.raises(fg.FP8GemmError):
+        fg.plan(256, 4096, 4096, Options(path=PATH_MAIN, mma_ctas=2, tile_n=64))
+    x, w, s = synth.make_inputs(200, 4100, 700, seed=8)
+    check_full(x, w, s, what="mid-M auto plan")
 
 
 PAIR_SHAPES = [
