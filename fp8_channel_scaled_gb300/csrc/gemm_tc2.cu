@@ -58,8 +58,12 @@ struct Cfg2 {
   static constexpr int kStageBytes = kABytes + kBBytes;  // [x kb0][x kb1][w kb0][w kb1]
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
   static constexpr int kStgOff = STAGES * kStageBytes;            // 4 warps x 2 staging boxes
-  static constexpr int kBarOff = kStgOff + kEpiWarps * 2 * kStgBytes;
   static constexpr int kNumBars = 2 * STAGES + 6 + kEpiWarps;  // + one per epilogue warp
+  // each epilogue warp's copy of the tile's BN scales, where it fits
+  static constexpr int kScOff = kStgOff + kEpiWarps * 2 * kStgBytes;
+  static constexpr bool kScInSmem =
+      1024 + kScOff + kEpiWarps * BN * 4 + kNumBars * 8 + 16 <= 232448;
+  static constexpr int kBarOff = kScOff + (kScInSmem ? kEpiWarps * BN * 4 : 0);
   static constexpr int kPartBytes = BN * 128;  // one warp's share of a partial sum (32 x BN fp32)
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
@@ -108,19 +112,20 @@ __device__ __forceinline__ void emit_chunk(const CUtensorMap* tmY, uint32_t buf,
 // Scale, round and store accumulator chunks [C0, C1) (32 columns each) of
 // one warp's 32 rows: TMEM address t_row, y rows [row0, row0 + 32) of which
 // those below row_end are the tile's, tile column block nb, scales from
-// scale[sbase + column]; chunk c is staged in box stg + (c - C0) * kStgBytes,
-// which no earlier store uses.
+// sc_s[column - nb BN] in shared memory (or, if sc_s is null, from
+// scale[sbase + column]); chunk c is staged in box stg + (c - C0) *
+// kStgBytes, which no earlier store uses.
 template <int BN, int C0, int C1>
 __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
                                              const CUtensorMap* tmY, const GemmArgs& p,
                                              int row0, int row_end, int nb, int sbase,
-                                             uint32_t lane, bool zero_acc) {
+                                             uint32_t lane, bool zero_acc, const float* sc_s) {
   static_assert(C0 < C1, "chunk range");
   float scv[C1 - C0];
 #pragma unroll
   for (int c = C0; c < C1; ++c) {
     const int col = nb * BN + c * 32 + static_cast<int>(lane);
-    scv[c - C0] = col < p.N ? __ldg(p.scale + sbase + col) : 0.f;
+    scv[c - C0] = (sc_s == nullptr && col < p.N) ? __ldg(p.scale + sbase + col) : 0.f;
   }
   uint32_t va[32], vb[32];
   tmem_ld_32x32b_x32(t_row + C0 * 32, va);
@@ -132,15 +137,29 @@ __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
       else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
     }
     const uint32_t* v = ((c - C0) & 1) ? vb : va;
-    const float sc = scv[c - C0];
     uint32_t packed[16];
+    if (sc_s != nullptr) {
+      const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
-      const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
-      const float a0 = zero_acc ? 0.f : __uint_as_float(v[2 * j]);
-      const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
-      packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
+      for (int j = 0; j < 8; ++j) {
+        const float4 s4 = scs[j];
+        const float a0 = zero_acc ? 0.f : __uint_as_float(v[4 * j]);
+        const float a1 = zero_acc ? 0.f : __uint_as_float(v[4 * j + 1]);
+        const float a2 = zero_acc ? 0.f : __uint_as_float(v[4 * j + 2]);
+        const float a3 = zero_acc ? 0.f : __uint_as_float(v[4 * j + 3]);
+        packed[2 * j] = pack_bf16x2(a0 * s4.x, a1 * s4.y);
+        packed[2 * j + 1] = pack_bf16x2(a2 * s4.z, a3 * s4.w);
+      }
+    } else {
+      const float sc = scv[c - C0];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+        const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+        const float a0 = zero_acc ? 0.f : __uint_as_float(v[2 * j]);
+        const float a1 = zero_acc ? 0.f : __uint_as_float(v[2 * j + 1]);
+        packed[j] = pack_bf16x2(a0 * s0, a1 * s1);
+      }
     }
     const uint32_t buf = stg + static_cast<uint32_t>(c - C0) * kStgBytes;
     const uint32_t rb = buf + lane * 64u;
@@ -182,6 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<volatile int*>(gbase + C::kBarOff + 8 * C::kNumBars + 4);
   auto sA = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes); };
   auto sB = [&](int s) { return sbase + static_cast<uint32_t>(s * C::kStageBytes + C::kABytes); };
+  // epilogue warp q's copy of the current tile's scales (when C::kScInSmem)
+  auto sc_of = [&](uint32_t q) {
+    return reinterpret_cast<float*>(gbase + C::kScOff + q * static_cast<uint32_t>(BN) * 4u);
+  };
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -315,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row0 = tg.row + static_cast<int>(rank) * 128 + static_cast<int>(quarter) * 32;
           const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * BN;
           const uint32_t stg = sbase + (kEpiWarps + (warp - kProdWarp0)) * C::kHalf * kStgBytes;
+          // the scales were staged by epilogue warp `quarter` before it
+          // arrived on last_bar
           store_chunks<BN, C::kHalf, BN / 32>(t_row, stg, &tmY, p, row0, tg.row_end, tg.nb,
-                                              tg.sbase, lane, num_kb == 0);
+                                              tg.sbase, lane, num_kb == 0,
+                                              C::kScInSmem ? sc_of(quarter) : nullptr);
           if (lane == 0) tma_store_wait_read<0>();
           __syncwarp();
         }
@@ -401,14 +427,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
       // is used (its registers are read only after the next tcgen05.wait::ld)
       uint32_t va[32], vb[32];
+      // An owner's scales (lane l: column l of every chunk) are fetched before
+      // its accumulator is ready, then copied to this warp's shared array so
+      // that each chunk reads them as four-float broadcasts.
+      float scv[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int col = nb * BN + c * 32 + static_cast<int>(lane);
+        scv[c] = (wu.owner && col < p.N) ? __ldg(p.scale + tg.sbase + col) : 0.f;
+      }
+      float* const sc_s = sc_of(warp);
+      auto stage_scales = [&]() {
+        if constexpr (C::kScInSmem) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) sc_s[c * 32 + lane] = scv[c];
+          __syncwarp();
+        }
+      };
       if (last && wu.owner && wu.q_end == pair + 1 && tma_y) {
         // ---- the last unit, shared with the producer warps (see there): the
         // operand ring is idle, each chunk gets its own staging box in it
         if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
         tc_fence_after_sync();
+        stage_scales();
         if (lane == 0) mbar_arrive(last_bar);
         store_chunks<BN, 0, C::kHalf>(t_row, sbase + warp * C::kHalf * kStgBytes, &tmY, p, row0,
-                                      tg.row_end, nb, tg.sbase, lane, zero_acc);
+                                      tg.row_end, nb, tg.sbase, lane, zero_acc,
+                                      C::kScInSmem ? sc_s : nullptr);
       } else if (!wu.owner) {
         // ---- a segment that does not hold the tile's first K block: publish
         // its fp32 partial sum for the owner
@@ -432,17 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) st_release_u64(p.flags + static_cast<size_t>(pair) * 8u + slot, p.epoch);
       } else {
         // ---- the tile's owner: own accumulator (+ the partial sums of
-        // workers pair+1 .. q_end-1, in that order) * scale -> bf16 -> y.
-        // Each lane's scale of every chunk is fetched before the accumulator
-        // is ready.
-        float scv[kChunks];
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          const int col = nb * BN + c * 32 + static_cast<int>(lane);
-          scv[c] = col < p.N ? __ldg(p.scale + tg.sbase + col) : 0.f;
-        }
+        // workers pair+1 .. q_end-1, in that order) * scale -> bf16 -> y
         if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
         tc_fence_after_sync();
+        stage_scales();
         // The partial sum of the first contributor is brought into shared
         // memory with one bulk copy: a tile with contributors is always its
         // owner's last unit, so the operand ring is idle (every MMA of the
@@ -493,13 +531,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
           }
           const int col0 = nb * BN + c * 32;
-          const float sc = scv[c];
           uint32_t packed[16];
+          if constexpr (C::kScInSmem) {
+            const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
-            const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
-            packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+            for (int j = 0; j < 8; ++j) {
+              const float4 s4 = scs[j];
+              packed[2 * j] = pack_bf16x2(a[4 * j] * s4.x, a[4 * j + 1] * s4.y);
+              packed[2 * j + 1] = pack_bf16x2(a[4 * j + 2] * s4.z, a[4 * j + 3] * s4.w);
+            }
+          } else {
+            const float sc = scv[c];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+              const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+              packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+            }
           }
           if (tma_y) {
             const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
