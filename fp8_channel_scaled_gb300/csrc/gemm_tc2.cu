@@ -47,6 +47,8 @@ constexpr int kProdWarp0 = 5;   // warps 5-8: x first half, x second half, w fir
 constexpr int kKbPerStage = 2;  // 128-byte K blocks per pipeline stage
 constexpr int kThreads = 288;
 constexpr int kStgBytes = 2048;  // one 32 x 32 bf16 staging box (64-byte swizzle)
+// tiles of at most this many K blocks take the rolled epilogue loop
+constexpr int kRolledEpilogueMaxKb = 12;
 
 template <int BN, int STAGES>
 struct Cfg2 {
@@ -173,7 +175,10 @@ __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
   }
 }
 
-template <int BN, int STAGES>
+// ROLLED: the owner epilogue's chunk loop is rolled (two chunks per
+// iteration) instead of fully unrolled; chosen for tiles of at most
+// kRolledEpilogueMaxKb K blocks (see the loop).
+template <int BN, int STAGES, bool ROLLED>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_linear_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
@@ -509,68 +514,148 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* staged_part =
             reinterpret_cast<const float*>(gbase + warp * C::kPartBytes) + lane;
         uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
-        tmem_ld_32x32b_x32(t_row, va);
+        if constexpr (ROLLED) {
+          // Short tiles (the epilogue, not the MMA, sets the pace): a rolled
+          // loop over chunk pairs (va, vb ping-pong) reuses the same
+          // instructions for every pair of chunks; fully unrolled, each chunk
+          // is new code that misses the instruction cache.  On long tiles the
+          // unrolled loop is kept: there the epilogue overlaps the next
+          // tile's MMAs, and a faster one takes issue slots from the MMA warp.
+          // one chunk: (partials added) * scale -> bf16 -> staged box -> TMA store
+          auto chunk = [&](int c, const uint32_t (&v)[32]) {
+            float a[32];
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c, ++chunk_no) {
-          tmem_ld_wait();
-          if (c + 1 < kChunks) {
-            if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
-            else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
-          }
-          const uint32_t* v = (c & 1) ? vb : va;
-          float a[32];
+            for (int j = 0; j < 32; ++j) a[j] = zero_acc ? 0.f : __uint_as_float(v[j]);
+            if (q_end > pair + 1) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] = zero_acc ? 0.f : __uint_as_float(v[j]);
-          if (q_end > pair + 1) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] += staged_part[(c * 32 + j) * 32];
-          }
-          for (int q = pair + 2; q < q_end; ++q) {
-            const float* src = part_of(q) + c * 1024 + lane;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
-          }
-          const int col0 = nb * BN + c * 32;
-          uint32_t packed[16];
-          if constexpr (C::kScInSmem) {
-            const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 s4 = scs[j];
-              packed[2 * j] = pack_bf16x2(a[4 * j] * s4.x, a[4 * j + 1] * s4.y);
-              packed[2 * j + 1] = pack_bf16x2(a[4 * j + 2] * s4.z, a[4 * j + 3] * s4.w);
+              for (int j = 0; j < 32; ++j) a[j] += staged_part[(c * 32 + j) * 32];
             }
-          } else {
-            const float sc = scv[c];
+            for (int q = pair + 2; q < q_end; ++q) {
+              const float* src = part_of(q) + c * 1024 + lane;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
-              const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
-              packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+              for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
             }
-          }
-          if (tma_y) {
-            const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
-            if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
-              if (lane == 0) tma_store_wait_read<1>();
+            const int col0 = nb * BN + c * 32;
+            uint32_t packed[16];
+            if constexpr (C::kScInSmem) {
+              const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 s4 = scs[j];
+                packed[2 * j] = pack_bf16x2(a[4 * j] * s4.x, a[4 * j + 1] * s4.y);
+                packed[2 * j + 1] = pack_bf16x2(a[4 * j + 2] * s4.z, a[4 * j + 3] * s4.w);
+              }
+            } else {
+              const float sc = scv[c];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+                const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+                packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+              }
+            }
+            if (tma_y) {
+              const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
+              if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
+                if (lane == 0) tma_store_wait_read<1>();
+                __syncwarp();
+              }
+              // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
+              const uint32_t rb = buf + lane * 64u;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+                       make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                  packed[4 * q + 3]));
+              fence_proxy_async_smem();
               __syncwarp();
+              emit_chunk(&tmY, buf, p, row0, tg.row_end, col0, lane, packed);
+            } else if (row < p.M && row < tg.row_end) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (col0 + j < p.N)
+                  yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
+                                                                 : (packed[j >> 1] & 0xFFFFu));
+              }
             }
-            // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
-            const uint32_t rb = buf + lane * 64u;
+            ++chunk_no;
+          };
+          tmem_ld_32x32b_x32(t_row, va);
+#pragma unroll 1
+          for (int c = 0; c < kChunks; c += 2) {
+            tmem_ld_wait();
+            if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+            chunk(c, va);
+            if (c + 1 < kChunks) {
+              tmem_ld_wait();
+              if (c + 2 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
+              chunk(c + 1, vb);
+            }
+          }
+        } else {
+          tmem_ld_32x32b_x32(t_row, va);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
-                     make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                                packed[4 * q + 3]));
-            fence_proxy_async_smem();
-            __syncwarp();
-            emit_chunk(&tmY, buf, p, row0, tg.row_end, col0, lane, packed);
-          } else if (row < p.M && row < tg.row_end) {
+          for (int c = 0; c < kChunks; ++c, ++chunk_no) {
+            tmem_ld_wait();
+            if (c + 1 < kChunks) {
+              if (c & 1) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, va);
+              else tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+            }
+            const uint32_t* v = (c & 1) ? vb : va;
+            float a[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < p.N)
-                yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
-                                                               : (packed[j >> 1] & 0xFFFFu));
+            for (int j = 0; j < 32; ++j) a[j] = zero_acc ? 0.f : __uint_as_float(v[j]);
+            if (q_end > pair + 1) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) a[j] += staged_part[(c * 32 + j) * 32];
+            }
+            for (int q = pair + 2; q < q_end; ++q) {
+              const float* src = part_of(q) + c * 1024 + lane;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
+            }
+            const int col0 = nb * BN + c * 32;
+            uint32_t packed[16];
+            if constexpr (C::kScInSmem) {
+              const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 s4 = scs[j];
+                packed[2 * j] = pack_bf16x2(a[4 * j] * s4.x, a[4 * j + 1] * s4.y);
+                packed[2 * j + 1] = pack_bf16x2(a[4 * j + 2] * s4.z, a[4 * j + 3] * s4.w);
+              }
+            } else {
+              const float sc = scv[c];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float s0 = __shfl_sync(0xffffffffu, sc, 2 * j);
+                const float s1 = __shfl_sync(0xffffffffu, sc, 2 * j + 1);
+                packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
+              }
+            }
+            if (tma_y) {
+              const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
+              if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
+                if (lane == 0) tma_store_wait_read<1>();
+                __syncwarp();
+              }
+              // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
+              const uint32_t rb = buf + lane * 64u;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+                       make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                  packed[4 * q + 3]));
+              fence_proxy_async_smem();
+              __syncwarp();
+              emit_chunk(&tmY, buf, p, row0, tg.row_end, col0, lane, packed);
+            } else if (row < p.M && row < tg.row_end) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (col0 + j < p.N)
+                  yrow[col0 + j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16)
+                                                                 : (packed[j >> 1] & 0xFFFFu));
+              }
             }
           }
         }
@@ -599,13 +684,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ dispatch
 struct Entry2 {
   int bn, stages;
-  const void* fn;
+  const void* fn;         // unrolled owner epilogue loop
+  const void* fn_rolled;  // rolled loop, for tiles of at most kRolledEpilogueMaxKb K blocks
   int smem;
 };
 
 template <int BN, int S>
 Entry2 make_entry2() {
-  return Entry2{BN, S, reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S>),
+  return Entry2{BN, S, reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, false>),
+                reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, true>),
                 Cfg2<BN, S>::kSmemBytes};
 }
 
@@ -641,7 +728,10 @@ int tc2_max_stages(int bn, int smem_optin) {
 cudaError_t tc2_prepare(int bn, int stages) {
   const Entry2* e = find2(bn, stages);
   if (!e) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
+  const cudaError_t r =
+      cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
+  if (r != cudaSuccess) return r;
+  return cudaFuncSetAttribute(e->fn_rolled, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
 }
 
 cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out) {
@@ -684,7 +774,8 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   GemmArgs args = a;
   int m2 = num_m2, nn = num_n, gm = c.group_m;
   void* params[] = {&mA, &mB, &mY, &args, &m2, &nn, &gm};
-  return cudaLaunchKernelExC(&cfg, e->fn, params);
+  return cudaLaunchKernelExC(&cfg, a.num_kb <= kRolledEpilogueMaxKb ? e->fn_rolled : e->fn,
+                             params);
 }
 
 }  // namespace fp8g
