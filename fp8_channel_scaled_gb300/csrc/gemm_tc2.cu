@@ -232,6 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Both CTAs' barriers are initialised before any cross-CTA arrive or TMA
+  // completion.
+  cluster_sync_all();
   // Global memory (operands, scales, y) is touched only after the preceding
   // grids of the stream have completed; the set-up above overlaps their tail.
   // Tensor memory is allocated only after the wait, so this CTA never holds
@@ -244,16 +247,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProdWarp0 && lane == 0) tma_prefetch_desc(&tmA);
   if (warp == kProdWarp0 + 2 && lane == 0) tma_prefetch_desc(&tmB);
   if (warp == 0 && lane == 0 && p.vec_store) tma_prefetch_desc(&tmY);
-  // both CTAs' barriers are initialised (and TMEM allocated) before any
-  // cross-CTA arrive or TMA completion
+  // Both CTAs' tensor memory is allocated before any MMA or tcgen05.ld: every
+  // thread arrives on a cluster barrier here; the MMA issuer and the epilogue
+  // wait for it at once, the producers (no tensor memory until the last
+  // unit) only after issuing their loads, so the first loads are in flight
+  // while the allocation completes.  Our dependents may launch once every
+  // CTA of this grid holds its tensor memory (each thread signals after its
+  // wait): a dependent CTA sharing an SM can then only wait for ours to free
+  // it, never take it first.
   tc_fence_before_sync();
-  cluster_sync_all();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *holder;
-  // Our dependents may launch once every CTA of this grid holds its tensor
-  // memory: a dependent CTA sharing an SM can then only wait for ours to
-  // free it, never take it first.
-  griddep_launch_dependents();
+  cluster_arrive_release();
+  uint32_t tmem_base = 0;
+  if (warp < kProdWarp0) {
+    cluster_wait_acquire();
+    tc_fence_after_sync();
+    tmem_base = *holder;
+    griddep_launch_dependents();
+  }
 
   const WaitCtx wc{p.err, abort_flag, p.budget_ns};
   // a fresh mapper per role: each walks the tile list forward once
@@ -319,6 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    cluster_wait_acquire();  // the allocation barrier (see above)
+    tc_fence_after_sync();
+    tmem_base = *holder;
+    griddep_launch_dependents();
     // ---- the last unit's epilogue is exposed (nothing overlaps it), so the
     // four producer warps, idle by then, store the second half of its chunks
     // for the 32 rows of their TMEM lane quarter (warp % 4); the epilogue
