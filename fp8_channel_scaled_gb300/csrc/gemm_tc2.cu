@@ -47,8 +47,8 @@ constexpr int kProdWarp0 = 5;   // warps 5-8: x first half, x second half, w fir
 constexpr int kKbPerStage = 2;  // 128-byte K blocks per pipeline stage
 constexpr int kThreads = 288;
 constexpr int kStgBytes = 2048;  // one 32 x 32 bf16 staging box (64-byte swizzle)
-// tiles of at most this many K blocks take the rolled epilogue loop
-constexpr int kRolledEpilogueMaxKb = 12;
+// tiles of at most this many K blocks (K <= 3072) take the rolled epilogue loop
+constexpr int kRolledEpilogueMaxKb = 24;
 
 template <int BN, int STAGES>
 struct Cfg2 {
