@@ -529,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<const float*>(gbase + warp * C::kPartBytes) + lane;
         uint16_t* yrow = p.y + static_cast<size_t>(row) * static_cast<size_t>(p.N);
         if constexpr (ROLLED) {
-          // Short tiles (the epilogue, not the MMA, sets the pace): a rolled
-          // loop over chunk pairs (va, vb ping-pong) reuses the same
+          // Short tiles (the epilogue, not the MMA, tends to set the pace): a
+          // rolled loop over chunk pairs (va, vb ping-pong) reuses the same
           // instructions for every pair of chunks; fully unrolled, each chunk
           // is new code that misses the instruction cache.  On long tiles the
-          // unrolled loop is kept: there the epilogue overlaps the next
-          // tile's MMAs, and a faster one takes issue slots from the MMA warp.
+          // epilogue hides behind the next tile's MMAs and either loop does
+          // (rolling them too moved those shapes by under 1%).
           // one chunk: (partials added) * scale -> bf16 -> staged box -> TMA store
           auto chunk = [&](int c, const uint32_t (&v)[32]) {
             float a[32];
