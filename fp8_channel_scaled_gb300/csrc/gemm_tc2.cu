@@ -536,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // epilogue hides behind the next tile's MMAs and either loop does
           // (rolling them too moved those shapes by under 1%).
           // one chunk: (partials added) * scale -> bf16 -> staged box -> TMA store
-          auto chunk = [&](int c, const uint32_t (&v)[32]) {
+          // a chunk's (partials added) * scale -> bf16, into packed
+          auto compute = [&](int c, const uint32_t (&v)[32], uint32_t (&packed)[16]) {
             float a[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = zero_acc ? 0.f : __uint_as_float(v[j]);
@@ -549,8 +550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) a[j] += __ldcg(src + j * 32);
             }
-            const int col0 = nb * BN + c * 32;
-            uint32_t packed[16];
             if constexpr (C::kScInSmem) {
               const float4* scs = reinterpret_cast<const float4*>(sc_s + c * 32);
 #pragma unroll
@@ -568,23 +567,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 packed[j] = pack_bf16x2(a[2 * j] * s0, a[2 * j + 1] * s1);
               }
             }
-            if (tma_y) {
-              const uint32_t buf = stg + (chunk_no & 1u) * kStgBytes;
-              if (chunk_no >= 2) {  // the store issued from this buffer two chunks ago
-                if (lane == 0) tma_store_wait_read<1>();
-                __syncwarp();
-              }
-              // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
-              const uint32_t rb = buf + lane * 64u;
+          };
+          // row `lane`, 16-byte chunk q at q ^ ((row >> 1) & 3): the 64-byte swizzle
+          auto put = [&](uint32_t buf, const uint32_t (&packed)[16]) {
+            const uint32_t rb = buf + lane * 64u;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
-                       make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                                  packed[4 * q + 3]));
-              fence_proxy_async_smem();
-              __syncwarp();
-              emit_chunk(&tmY, buf, p, row0, tg.row_end, col0, lane, packed);
-            } else if (row < p.M && row < tg.row_end) {
+            for (int q = 0; q < 4; ++q)
+              sts_v4(rb + ((static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4),
+                     make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                packed[4 * q + 3]));
+          };
+          auto direct = [&](int c, const uint32_t (&packed)[16]) {
+            const int col0 = nb * BN + c * 32;
+            if (row < p.M && row < tg.row_end) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 if (col0 + j < p.N)
@@ -592,19 +587,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                  : (packed[j >> 1] & 0xFFFFu));
               }
             }
-            ++chunk_no;
           };
+          // Chunks are handled in pairs (va, vb ping-pong): both are
+          // computed, then staged in the warp's two boxes once the previous
+          // pair's stores have read them, with one proxy fence for the two.
           tmem_ld_32x32b_x32(t_row, va);
 #pragma unroll 1
           for (int c = 0; c < kChunks; c += 2) {
+            const bool two = c + 1 < kChunks;
+            uint32_t pk0[16], pk1[16];
             tmem_ld_wait();
-            if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
-            chunk(c, va);
-            if (c + 1 < kChunks) {
+            if (two) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+            compute(c, va, pk0);
+            if (two) {
               tmem_ld_wait();
               if (c + 2 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
-              chunk(c + 1, vb);
+              compute(c + 1, vb, pk1);
             }
+            if (tma_y) {
+              if (chunk_no > 0) {  // every earlier store has read its box
+                if (lane == 0) tma_store_wait_read<0>();
+                __syncwarp();
+              }
+              put(stg, pk0);
+              if (two) put(stg + kStgBytes, pk1);
+              fence_proxy_async_smem();
+              __syncwarp();
+              emit_chunk(&tmY, stg, p, row0, tg.row_end, nb * BN + c * 32, lane, pk0);
+              if (two)
+                emit_chunk(&tmY, stg + kStgBytes, p, row0, tg.row_end, nb * BN + (c + 1) * 32,
+                           lane, pk1);
+            } else {
+              direct(c, pk0);
+              if (two) direct(c + 1, pk1);
+            }
+            chunk_no += two ? 2u : 1u;
           }
         } else {
           tmem_ld_32x32b_x32(t_row, va);
