@@ -22,7 +22,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -102,17 +101,19 @@ def sources_sha(paths) -> str:
 
 
 def recorded_traffic(workload: str, paths):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    fn = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    """DRAM bytes (read + write) per launch of the workload's GEMM kernel from
+    the committed ncu record, if it was taken on the current kernel source;
+    else None."""
+    fn = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
-        text = open(fn).read()
-    except OSError:
+        with open(fn) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
         return None
     sha = sources_sha(paths)
-    for m in re.finditer(r"^\|\s*(\w+)\s*\|\s*([0-9a-f]{16})\s*\|\s*(\d+)\s*\|", text, re.M):
-        if m.group(1) == workload and m.group(2) == sha:
-            return int(m.group(3))
+    for e in entries:
+        if e.get("workload") == workload and e.get("sources_sha") == sha:
+            return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
     return None
 
 
@@ -468,6 +469,8 @@ def run_ours(args):
             gbs = wl2.algorithmic_bytes / k2 / 1e9
             roof_t = max(wl2.flops / 4.5e15, wl2.algorithmic_bytes / 8e12)
             p2 = fg.plan(wl2.M, wl2.N, wl2.K, x=sets2[0][0], w=sets2[0][1])
+            srcs2 = (DEC_SOURCES if p2.path == fg.PATH_DECODE
+                     else TC2_SOURCES if p2.cluster == 2 else TC_SOURCES)
             others[key2] = {"workload": wl2.name + (" (w prepared once to a 16-byte pitch; x repitched per call)" if key2 != base else ""),
                             "us_per_call": round(k2 * 1e6, 2),
                            "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1),
@@ -477,6 +480,7 @@ def run_ours(args):
                            "path": "main" if p2.path == fg.PATH_MAIN else "decode",
                            "splits": p2.splits, "realign": p2.realign,
                            "launches": p2.launches,
+                           "traffic": recorded_traffic(key2, srcs2) if key2 == base else None,
                            "l2": "no rotation (launch-bound)" if key2 == "small" else f"rotating {len(sets2)} sets"}
             del sets2
             torch.cuda.empty_cache()

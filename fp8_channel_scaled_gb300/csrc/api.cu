@@ -93,8 +93,42 @@ const int kTc2Stages[] = {3, 4};
 const int kDecMp[] = {32, 64, 128};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
+// Makes device `dev` current for the guard's lifetime and makes the caller's
+// current device current again when it ends, so that no entry point leaves a
+// different device current than it found (nothing is switched when `dev` is
+// already current).
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+    if (prev_ == dev) {
+      ok_ = true;
+    } else if (cudaSetDevice(dev) == cudaSuccess) {
+      ok_ = true;
+      switched_ = prev_ >= 0;
+    } else {
+      cudaGetLastError();
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_ && cudaSetDevice(prev_) != cudaSuccess) cudaGetLastError();
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = false;
+  bool switched_ = false;
+};
+
 // Per-device set-up, once: properties, error word address, kernel attributes.
 // It allocates nothing; the workspace pool is created on first pooled use.
+// Device `dev` must be current (the callers hold a DeviceGuard).
 int device_state(int dev, DevState** out) {
   if (dev < 0 || dev >= kMaxDevices) return FP8GEMM_EDEVICE;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -107,8 +141,7 @@ int device_state(int dev, DevState** out) {
   std::memset(d.dec_clusters, 0xff, sizeof(d.dec_clusters));
   d.status = FP8GEMM_EDEVICE;
   int major = 0, minor = 0;
-  if (cudaSetDevice(dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -683,13 +716,11 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   if (dev < 0 || pointer_device(scale) != dev ||
       (K > 0 && (pointer_device(x) != dev || pointer_device(w) != dev)))
     return FP8GEMM_EINVAL;
+  const DeviceGuard guard(dev);
+  if (!guard.ok()) return FP8GEMM_EDEVICE;
   DevState* d = nullptr;
   int st = device_state(dev, &d);
   if (st != FP8GEMM_OK) return st;
-  if (cudaSetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
-  }
   Plan pl;
   st = make_plan(*d, x, w, M, N, K, opt, &pl);
   if (st != FP8GEMM_OK) return st;
@@ -755,13 +786,11 @@ extern "C" int fp8_gemm_scaled_noalloc(const void* x, const void* w, const float
   if (dev < 0 || pointer_device(scale) != dev ||
       (K > 0 && (pointer_device(x) != dev || pointer_device(w) != dev)))
     return FP8GEMM_EINVAL;
+  const DeviceGuard guard(dev);
+  if (!guard.ok()) return FP8GEMM_EDEVICE;
   DevState* d = nullptr;
   int st = device_state(dev, &d);
   if (st != FP8GEMM_OK) return st;
-  if (cudaSetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
-  }
   uint8_t* ws = nullptr;
   st = noalloc_workspace(*d, &ws);
   if (st != FP8GEMM_OK) return st;
@@ -790,13 +819,11 @@ extern "C" int fp8_gemm_prepare_weight(const void* w, int N, int K, void* w_out,
   if (overlaps(w, wb, w_out, ob)) return FP8GEMM_EINVAL;
   const int dev = pointer_device(w_out);
   if (dev < 0 || pointer_device(w) != dev) return FP8GEMM_EINVAL;
+  const DeviceGuard guard(dev);
+  if (!guard.ok()) return FP8GEMM_EDEVICE;
   DevState* d = nullptr;
   int st = device_state(dev, &d);
   if (st != FP8GEMM_OK) return st;
-  if (cudaSetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
-  }
   RepitchArgs r{};
   r.w = static_cast<const uint8_t*>(w);
   r.wo = static_cast<uint8_t*>(w_out);
@@ -838,13 +865,11 @@ extern "C" int fp8_gemm_grouped(const void* x, const void* w, const float* scale
   if (dev < 0 || pointer_device(scale) != dev || pointer_device(x) != dev ||
       pointer_device(w) != dev || pointer_device(offsets) != dev)
     return FP8GEMM_EINVAL;
+  const DeviceGuard guard(dev);
+  if (!guard.ok()) return FP8GEMM_EDEVICE;
   DevState* d = nullptr;
   int st = device_state(dev, &d);
   if (st != FP8GEMM_OK) return st;
-  if (cudaSetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return FP8GEMM_ELAUNCH;
-  }
   // CTA-pair tiles chosen as for one group of M rows; the work list (tiles of
   // every group) is built on the device, so every resident pair is launched.
   fp8gemm_options o;
@@ -879,6 +904,9 @@ extern "C" int fp8_gemm_scaled(const void* x, const void* w, const float* scale,
 extern "C" int fp8_gemm_plan(int device, const void* x, const void* w, int M, int N, int K,
                              const fp8gemm_options* opt, fp8gemm_plan* out) {
   if (!out || M < 0 || N < 0 || K < 0) return FP8GEMM_EINVAL;
+  if (device < 0 || device >= kMaxDevices) return FP8GEMM_EDEVICE;
+  const DeviceGuard guard(device);
+  if (!guard.ok()) return FP8GEMM_EDEVICE;
   DevState* d = nullptr;
   int st = device_state(device, &d);
   if (st != FP8GEMM_OK) return st;

@@ -33,6 +33,10 @@
  *     padded-input failure, "qwen3.8-max" page, odd-K pad-cache paragraph,
  *     is impossible by construction).
  *   - Thread safety: calls may come from several host threads.
+ *   - Devices: a call works on the device that holds y (all buffers must be
+ *     on it).  It makes that device current only while it runs and makes the
+ *     caller's current device current again before it returns, on every
+ *     return path; fp8_gemm_plan does the same for its `device` argument.
  *   - CUDA graphs: a call that takes no workspace from the pool (operands
  *     TMA can tile, or a caller workspace) enqueues kernel launches only and
  *     can be captured into a graph once the device has been set up by an

@@ -630,6 +630,51 @@ def test_rejects_host_pointers_and_aliasing():
     assert fg.fp8_gemm_check_device_error() == 0
 
 
+def test_entry_points_leave_the_current_device_unchanged():
+    """Each entry point makes the device that holds y current only for the
+    call: the caller's current device is current again when it returns.  Data
+    on device d is used while device (d + 1) % n is current; on a one-GPU
+    machine that is the same device, and the check is that it stays current."""
+    import ctypes
+    lib = fg.lib()
+    vp = ctypes.c_void_p
+    n = torch.cuda.device_count()
+    for d in range(n):
+        other = (d + 1) % n
+        dev = torch.device("cuda", d)
+        M, N, K = 64, 256, 4127
+        x, w, s = synth.make_inputs(M, N, K, 21)
+        xd, wd, sd = (torch.from_numpy(a).to(dev) for a in (x, w, s))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wp = torch.empty((N, 4128), dtype=torch.uint8, device=dev)
+        xa = torch.zeros((M, 4128), dtype=torch.uint8, device=dev)
+        offs = torch.tensor([0, M], dtype=torch.int32, device=dev)
+        p = [vp(t.data_ptr()) for t in (xd, wd, sd, y)]
+        opts = Options(mma_ctas=2, path=PATH_MAIN)._c()
+        plan = fg._binding._CPlan()
+        torch.cuda.set_device(other)
+        calls = [
+            ("scaled", lambda: lib.fp8_gemm_scaled(*p, M, N, K, None)),
+            ("scaled_ex", lambda: lib.fp8_gemm_scaled_ex(*p, M, N, K, ctypes.byref(opts), None)),
+            ("noalloc", lambda: lib.fp8_gemm_scaled_noalloc(*p, M, N, K, None)),
+            ("prepare_weight", lambda: lib.fp8_gemm_prepare_weight(
+                p[1], N, K, vp(wp.data_ptr()), 4128, None)),
+            ("grouped", lambda: lib.fp8_gemm_grouped(
+                vp(xa.data_ptr()), vp(wp.data_ptr()), p[2], p[3], vp(offs.data_ptr()), 1, M, N,
+                4128, None, None)),
+            ("plan", lambda: lib.fp8_gemm_plan(d, None, None, M, N, K, None, ctypes.byref(plan))),
+        ]
+        for name, call in calls:
+            assert call() == 0, name
+            assert torch.cuda.current_device() == other, name
+        torch.cuda.set_device(d)
+        assert fg.fp8_gemm_check_device_error() == 0
+        # the last output written is the grouped layer's on the prepared
+        # weight with zero x: every element is zero
+        assert bool(torch.all(y == 0))
+    torch.cuda.set_device(0)
+
+
 # ------------------------------------------------------------------ CUDA graph capture
 @pytest.mark.parametrize("M,N,K", [(64, 128, 256), (512, 1024, 512), (32, 2048, 1024)])
 def test_cuda_graph_capture_and_replay_with_new_data(M, N, K):
