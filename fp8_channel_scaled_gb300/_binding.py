@@ -12,7 +12,7 @@ _LIB_PATH = _PKG / "_lib" / "libfp8gemm.so"
 
 PATH_AUTO, PATH_MAIN, PATH_DECODE = 0, 1, 2
 STATUS = {0: "OK", 1: "EINVAL", 2: "EALIGN", 3: "EDEVICE", 4: "ELAUNCH", 5: "ETIMEOUT",
-          6: "EUNSUPPORTED", 7: "ESIZE"}
+          6: "EUNSUPPORTED", 7: "ESIZE", 8: "ENOMEM"}
 NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 

@@ -45,6 +45,15 @@ __global__ void selftest_wait_kernel(unsigned* err, unsigned long long budget_ns
 }
 
 constexpr int kMaxDevices = 64;
+// Streams per device that keep a workspace; calls on further streams take
+// theirs from the pool for the call.
+constexpr int kStreamWorkspaces = 16;
+
+struct StreamWorkspace {
+  unsigned long long stream_id = 0;
+  uint8_t* ptr = nullptr;
+  size_t bytes = 0;
+};
 constexpr unsigned long long kDefaultBudgetNs = 1000000000ull;
 
 struct DevState {
@@ -53,9 +62,18 @@ struct DevState {
   int sm_count = 0;
   int smem_optin = 0;
   unsigned* err_word = nullptr;
-  cudaMemPool_t pool = nullptr;  // private stream-ordered pool for repitch workspaces,
-  bool pool_failed = false;      // created on first pooled use, never by the no-alloc entry
+  cudaMemPool_t pool = nullptr;  // private stream-ordered pool the shared workspace comes
+  bool pool_failed = false;      // from; created on first use, never by the no-alloc entry
   void* noalloc_ws = nullptr;    // device address of g_noalloc_workspace on this device
+  // Workspaces of the calls that bring none (repitch copies, split-tail
+  // partial sums), one per stream: created on a stream's first need, grown
+  // (in that stream's order) when a call needs more, kept until exit.  Calls
+  // on one stream are ordered by the stream, so no two kernels that use the
+  // same workspace ever overlap.  Streams are told apart by cudaStreamGetId,
+  // which is never reused within a process.
+  std::mutex ws_mu;
+  StreamWorkspace ws[kStreamWorkspaces];
+  int ws_count = 0;
   // Occupancy of each kernel configuration, queried once on first use so that
   // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
   int tc2_pairs[6][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
@@ -212,6 +230,47 @@ cudaMemPool_t workspace_pool(DevState& d, int dev) {
   return d.pool;
 }
 
+// The workspace kept for stream `s` (id `sid`), grown to at least `need`
+// bytes; nullptr in *out (and FP8GEMM_OK) when the device already keeps
+// workspaces for kStreamWorkspaces other streams.  Growing frees the old
+// block and takes the new one on `s`, i.e. after every earlier kernel of `s`,
+// the only ones that used it.  The caller holds d.ws_mu until it has enqueued
+// its kernels.  FP8GEMM_ENOMEM if the pool cannot provide the memory.
+int stream_workspace(DevState& d, int dev, unsigned long long sid, size_t need, cudaStream_t s,
+                     uint8_t** out) {
+  *out = nullptr;
+  StreamWorkspace* e = nullptr;
+  for (int i = 0; i < d.ws_count; ++i)
+    if (d.ws[i].stream_id == sid) e = &d.ws[i];
+  if (!e) {
+    if (d.ws_count == kStreamWorkspaces) return FP8GEMM_OK;
+    e = &d.ws[d.ws_count++];
+    e->stream_id = sid;
+  }
+  if (e->bytes < need) {
+    cudaMemPool_t pool = workspace_pool(d, dev);
+    if (!pool) return FP8GEMM_ENOMEM;
+    if (e->ptr) {
+      if (cudaFreeAsync(e->ptr, s) != cudaSuccess) cudaGetLastError();
+      e->ptr = nullptr;
+      e->bytes = 0;
+    }
+    // a quarter more than asked, in whole 2 MiB pages, so that a few
+    // slightly larger calls do not each grow it
+    const size_t grain = size_t(2) << 20;
+    const size_t want = ((need + need / 4) + grain - 1) / grain * grain;
+    void* p = nullptr;
+    if (cudaMallocFromPoolAsync(&p, want, pool, s) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return FP8GEMM_ENOMEM;
+    }
+    e->ptr = static_cast<uint8_t*>(p);
+    e->bytes = want;
+  }
+  *out = e->ptr;
+  return FP8GEMM_OK;
+}
+
 template <typename T, size_t n>
 int index_of(const T (&arr)[n], T v) {
   for (size_t i = 0; i < n; ++i)
@@ -334,6 +393,32 @@ int tail_workers_for(long long tiles, int pairs, int num_kb) {
   return tw > rem ? static_cast<int>(tw) : 0;
 }
 
+// Whether the next kernel on `s` may be launched with programmatic stream
+// serialization: always outside a stream capture; during one only when every
+// node the launch will depend on is a kernel node, because a programmatic
+// edge can only leave a kernel (after a copy, memset, event or memory node,
+// e.g. a workspace allocation, the launch takes an ordinary edge).
+bool pdl_ok(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t n = 0;
+  if (cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, nullptr, &n) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (cs == cudaStreamCaptureStatusNone) return true;
+  if (cs != cudaStreamCaptureStatusActive || n == 0 || !deps) return false;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(deps[i], &t) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (t != cudaGraphNodeTypeKernel) return false;
+  }
+  return true;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
 
@@ -431,7 +516,7 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   // too: the in-kernel loader holds its loads in registers and cannot keep
   // enough in flight; M = 32, N = 4096, K = 4127: 15.2 us repitched against
   // 21.4 us, N = K = 8191: 37.4 against 41.6 us.)
-  const bool can_ws = !o.no_workspace && (o.workspace || !d.pool_failed);
+  const bool can_ws = !o.no_workspace;
   const bool repitch = K > 0 && !tma_ok && !o.force_realign && can_ws;
   // K == 0 has nothing to load; the realigning variant then issues no copy
   // and needs no tensor map.
@@ -587,6 +672,7 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const v
   a.budget_ns = budget_ns();
   a.group_offsets = group_offsets;
   a.groups = groups;
+  a.pdl = pdl_ok(s) ? 1 : 0;
   // a grouped layer's weight is [groups * N, K]
   const int w_rows = group_offsets ? groups * N : N;
   if (pl.pub.path == FP8GEMM_PATH_MAIN && pl.tc.tail_workers > 0) {
@@ -679,6 +765,7 @@ int run_with_workspace(const Plan& pl, DevState& d, const void* x, size_t ldx, c
   r.rows_w = pl.rw ? N : 0;
   r.ldx = static_cast<long long>(ldx);
   r.ldw = static_cast<long long>(ldw);
+  r.pdl = pdl_ok(s) ? 1 : 0;
   if (launch_repitch(r, s) != cudaSuccess) {
     cudaGetLastError();
     return FP8GEMM_ELAUNCH;
@@ -729,37 +816,49 @@ extern "C" int fp8_gemm_scaled_ex(const void* x, const void* w, const float* sca
   if (need == 0) return launch_gemm(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, nullptr, s);
 
   // workspace (repitch copies and/or split-tail partial sums): the caller's,
-  // or stream-ordered from the device's pool
-  uint8_t* ws = nullptr;
-  bool pooled = false;
+  // else the one the device keeps for this stream, else (while the stream is
+  // being captured into a CUDA graph, whose replays may run on any stream,
+  // or when the device keeps workspaces for too many other streams) one
+  // taken for this call in stream order
   if (opt && opt->workspace) {
-    ws = static_cast<uint8_t*>(opt->workspace);
+    uint8_t* ws = static_cast<uint8_t*>(opt->workspace);
     if (opt->workspace_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
         pointer_device(ws) != dev || overlaps(ws, need, y, yb) || overlaps(ws, need, x, xb) ||
         overlaps(ws, need, w, wb) || overlaps(ws, need, scale, sb))
       return FP8GEMM_EINVAL;
-  } else {
-    void* p = nullptr;
-    cudaMemPool_t pool = workspace_pool(*d, dev);
-    if (!pool || cudaMallocFromPoolAsync(&p, need, pool, s) != cudaSuccess) {
-      // no memory for a workspace: load unaligned rows in the kernel (and
-      // run the last wave unsplit) instead
-      cudaGetLastError();
-      fp8gemm_options o2;
-      std::memset(&o2, 0, sizeof(o2));
-      if (opt) o2 = *opt;
-      o2.no_workspace = 1;
-      o2.workspace = nullptr;
-      o2.workspace_bytes = 0;
-      st = make_plan(*d, x, w, M, N, K, &o2, &pl);
-      if (st != FP8GEMM_OK) return st;
-      return launch_gemm(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, nullptr, s);
-    }
-    ws = static_cast<uint8_t*>(p);
-    pooled = true;
+    return run_with_workspace(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, ws, s);
   }
-  st = run_with_workspace(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, ws, s);
-  if (pooled && cudaFreeAsync(ws, s) != cudaSuccess) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8GEMM_ELAUNCH;
+  }
+  if (cap == cudaStreamCaptureStatusNone) {
+    unsigned long long sid = 0;
+    if (cudaStreamGetId(s, &sid) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8GEMM_ELAUNCH;
+    }
+    std::lock_guard<std::mutex> lk(d->ws_mu);
+    uint8_t* ws = nullptr;
+    st = stream_workspace(*d, dev, sid, need, s, &ws);
+    if (st != FP8GEMM_OK) return st;
+    if (ws) return run_with_workspace(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, ws, s);
+  }
+  void* p = nullptr;
+  const cudaError_t ae = cap == cudaStreamCaptureStatusNone
+                             ? [&]() {
+                                 cudaMemPool_t pool = workspace_pool(*d, dev);
+                                 return pool ? cudaMallocFromPoolAsync(&p, need, pool, s)
+                                             : cudaErrorMemoryAllocation;
+                               }()
+                             : cudaMallocAsync(&p, need, s);
+  if (ae != cudaSuccess || !p) {
+    cudaGetLastError();
+    return FP8GEMM_ENOMEM;
+  }
+  st = run_with_workspace(pl, *d, x, ldx, w, ldw, K, scale, y, M, N, static_cast<uint8_t*>(p), s);
+  if (cudaFreeAsync(p, s) != cudaSuccess) {
     cudaGetLastError();
     if (st == FP8GEMM_OK) st = FP8GEMM_ELAUNCH;
   }
@@ -832,6 +931,7 @@ extern "C" int fp8_gemm_prepare_weight(const void* w, int N, int K, void* w_out,
   r.rows_x = 0;
   r.rows_w = N;
   r.ldw = K;
+  r.pdl = pdl_ok(reinterpret_cast<cudaStream_t>(stream)) ? 1 : 0;
   if (launch_repitch(r, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return FP8GEMM_ELAUNCH;
@@ -989,6 +1089,9 @@ extern "C" const char* fp8_gemm_status_string(int status) {
     case FP8GEMM_ESIZE:
       return "fp8_gemm_scaled_noalloc: the repitch workspace this call needs exceeds "
              "FP8GEMM_NOALLOC_WORKSPACE_BYTES";
+    case FP8GEMM_ENOMEM:
+      return "no device memory for the workspace this call needs (pass one in "
+             "fp8gemm_options.workspace, or set no_workspace)";
     default: return "unknown status";
   }
 }

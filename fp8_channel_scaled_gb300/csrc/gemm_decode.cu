@@ -111,10 +111,23 @@ __global__ void __launch_bounds__(kThreads)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Global memory (operands, scales, y) is touched only after the preceding
-  // grids of the stream have completed; the set-up above overlaps their tail.
-  // Tensor memory is allocated only after the wait, so this CTA never holds
-  // it while it waits for another grid.
+  // While the preceding grid of the stream drains, the TMA issuers ask L2 for
+  // this CTA's first STAGES boxes of w: a prefetch delivers nothing to the
+  // CTA, so the loads issued after the dependency wait below still observe
+  // every write of the preceding grids, but the weight stream starts from L2
+  // instead of paying the DRAM latency after the wait (decode 32 x 8192 x
+  // 8192: 15.5 -> 14.6 us per call back to back; prefetching the first 16
+  // boxes instead gained less, 14.9 us).
+  if (!REALIGN && lane == 0 && static_cast<int>(warp) < issuers_for<STAGES>()) {
+    tma_prefetch_desc(&tmW);
+    const int pf = my_kb < STAGES ? my_kb : STAGES;
+    for (int i = static_cast<int>(warp); i < pf; i += issuers_for<STAGES>())
+      tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBK, n0);
+  }
+  // Global memory (operands, scales, y) is read or written only after the
+  // preceding grids of the stream have completed; the set-up above overlaps
+  // their tail.  Tensor memory is allocated only after the wait, so this CTA
+  // never holds it while it waits for another grid.
   griddep_wait();
   if (warp == kMmaWarp) {
     tmem_alloc(holder_addr, C::kTmemCols);
@@ -423,7 +436,7 @@ cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   attr[0].val.clusterDim.z = 1;
   set_pdl(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   CUtensorMap mA = tmA, mB = tmB;
   GemmArgs args = a;
   int splits = c.splits;

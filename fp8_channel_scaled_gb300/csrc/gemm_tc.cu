@@ -386,7 +386,7 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
   cudaLaunchAttribute attr[1];
   set_pdl(attr[0]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, e->fn, params);
 }
 

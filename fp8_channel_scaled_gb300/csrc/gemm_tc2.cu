@@ -800,7 +800,7 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   attr[0].val.clusterDim.z = 1;
   set_pdl(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   CUtensorMap mA = tmA, mB = tmB, mY = tmY;
   GemmArgs args = a;
   int m2 = num_m2, nn = num_n, gm = c.group_m;

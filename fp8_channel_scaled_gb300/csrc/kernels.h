@@ -36,6 +36,7 @@ struct GemmArgs {
   // The offsets are read on the device; values outside [0, M] are clamped.
   const int* group_offsets;  // device, groups + 1 entries
   int groups;
+  int pdl;  // host side: launch with programmatic stream serialization
 };
 
 // ---- persistent tcgen05 kernel (large M) ---------------------------------
@@ -72,6 +73,8 @@ cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
 // prologue, while the previous kernel of the stream is still finishing.  Each
 // kernel of this library waits in griddep_wait() before it touches global
 // memory, so stream order still holds for every byte it reads or writes.
+// Launches use it only when the host allows it for the stream (see pdl_ok in
+// api.cu): during stream capture a programmatic edge can only leave a kernel.
 inline void set_pdl(cudaLaunchAttribute& attr) {
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
@@ -107,6 +110,7 @@ struct RepitchArgs {
   long long rows_x;      // M, or 0 to leave x alone
   long long rows_w;      // N, or 0 to leave w alone
   long long ldx, ldw;    // source row pitches (>= K)
+  int pdl;               // launch with programmatic stream serialization
 };
 cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s);
 

@@ -243,6 +243,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// Prefetch one box of a tiled tensor into L2: no shared-memory destination,
+// no completion to wait for, no value returned to the thread.  L2 is the
+// point of coherence for device memory, so a box prefetched before the
+// preceding grid has finished writing it still reads as written by the
+// later loads.  c0 (bytes) must be a multiple of 16.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1) {

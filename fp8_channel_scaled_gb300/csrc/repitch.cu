@@ -104,7 +104,7 @@ cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   set_pdl(attr[0]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   switch (best_u) {
     case 2: return cudaLaunchKernelEx(&cfg, repitch_kernel<2>, a, segs);
     case 3: return cudaLaunchKernelEx(&cfg, repitch_kernel<3>, a, segs);

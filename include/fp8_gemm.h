@@ -21,13 +21,23 @@
  *     respect to the host and never synchronise.
  *   - Ownership: the caller owns every buffer.  The library keeps, per
  *     device, its properties, a 4-byte device error word (see
- *     fp8_gemm_check_device_error) and a private stream-ordered memory pool.
- *     The only device memory a call may take is the main path's workspace
- *     (see fp8_gemm_workspace_bytes): repitched copies of x and w, and the
- *     split tail's partial sums.  It comes from the caller when
- *     fp8gemm_options.workspace is given, else from that pool with
- *     cudaMallocFromPoolAsync / cudaFreeAsync on the call's stream, so calls
- *     on different streams never share it.
+ *     fp8_gemm_check_device_error) and a few workspaces.  A call needs a
+ *     workspace (see fp8_gemm_workspace_bytes) only for repitched copies of
+ *     x and w whose rows TMA cannot tile, and for the optional split tail's
+ *     partial sums.  It uses the caller's when fp8gemm_options.workspace is
+ *     given.  Otherwise it uses the workspace the device keeps for the
+ *     call's stream: taken from a private stream-ordered pool on that
+ *     stream's first such call, enlarged in the stream's order when a call
+ *     needs more, and kept until the process exits, so later calls on the
+ *     stream allocate nothing; calls on one stream are ordered by the stream,
+ *     so they never use it at the same time.  Streams are told apart by
+ *     cudaStreamGetId.  Workspaces are kept for at most 16 streams per
+ *     device; a call on a further stream, or on a stream being captured into
+ *     a CUDA graph (whose replays may run on any stream), takes its workspace
+ *     for itself in stream order (cudaMallocFromPoolAsync / cudaMallocAsync
+ *     and cudaFreeAsync; a capture records these as graph memory nodes).  If
+ *     the memory cannot be had the call returns FP8GEMM_ENOMEM and launches
+ *     nothing.
  *   - Nothing derived from the data is ever cached: each call reads x, w
  *     and weight_scale as they are when the kernel runs (the pages' stale
  *     padded-input failure, "qwen3.8-max" page, odd-K pad-cache paragraph,
@@ -37,10 +47,10 @@
  *     on it).  It makes that device current only while it runs and makes the
  *     caller's current device current again before it returns, on every
  *     return path; fp8_gemm_plan does the same for its `device` argument.
- *   - CUDA graphs: a call that takes no workspace from the pool (operands
- *     TMA can tile, or a caller workspace) enqueues kernel launches only and
- *     can be captured into a graph once the device has been set up by an
- *     earlier call; replays read the buffers as they are then.  Consecutive
+ *   - CUDA graphs: a call can be captured into a graph once the device has
+ *     been set up by an earlier call; replays read the buffers as they are
+ *     then.  A captured call that needs a workspace and brings none records
+ *     its own allocation in the graph (see Ownership).  Consecutive
  *     calls on a stream are launched with programmatic stream serialization:
  *     each kernel may start its set-up while the previous one drains, and
  *     touches global memory only after it has completed.
@@ -58,7 +68,7 @@ extern "C" {
  * (identical to cudaStream_t). */
 typedef struct CUstream_st *fp8gemm_stream_t;
 
-#define FP8GEMM_VERSION 3
+#define FP8GEMM_VERSION 4
 
 typedef enum {
     FP8GEMM_OK = 0,
@@ -68,8 +78,9 @@ typedef enum {
     FP8GEMM_ELAUNCH = 4,   /* the CUDA launch (or a CUDA runtime call) failed */
     FP8GEMM_ETIMEOUT = 5,  /* a kernel gave up a bounded wait (results invalid) */
     FP8GEMM_EUNSUPPORTED = 6, /* the options ask for a configuration not built */
-    FP8GEMM_ESIZE = 7      /* fp8_gemm_scaled_noalloc: workspace needed exceeds
+    FP8GEMM_ESIZE = 7,     /* fp8_gemm_scaled_noalloc: workspace needed exceeds
                               FP8GEMM_NOALLOC_WORKSPACE_BYTES */
+    FP8GEMM_ENOMEM = 8     /* no device memory for the workspace the call needs */
 } fp8gemm_status;
 
 /* Kernel path. */
@@ -149,12 +160,13 @@ typedef struct {
  *
  * Rows whose pitch K is not a multiple of 16 bytes (e.g. K = 4127), or
  * operands not 16-byte aligned, cannot be tiled by TMA.  They are first
- * copied by a repitch kernel into a workspace with a 16-byte pitch and zero
- * pad bytes (two launches); with no_workspace (or when no workspace memory
- * can be had) an in-kernel realigning producer loads them directly.
+ * copied by a repitch kernel into the workspace with a 16-byte pitch and zero
+ * pad bytes (two launches); with no_workspace an in-kernel realigning
+ * producer loads them directly instead (one launch, no workspace, but about
+ * ten times slower on large shapes: its loads pass through registers).
  * Either way bytes past K count as zeros, which adds exactly nothing (the
  * zero-padding argument of the "Kimi K3 (256k)" page, SM100 Triton
- * paragraph).  Nothing is cached between calls.
+ * paragraph).  No operand data is kept between calls.
  *
  * With fp8gemm_options.split_tail on CTA-pair tiles, when the tiles do not
  * fill the last wave of the persistent grid, that wave's tiles are cut along

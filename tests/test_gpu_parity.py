@@ -369,8 +369,9 @@ def test_long_k(M, N, path):
 # ------------------------------------------------------------------ concurrent host threads
 def test_concurrent_host_threads_on_separate_streams():
     # The binding releases the GIL inside each C call, so these threads enter
-    # the library at the same time: plan caches, the workspace pool (the
-    # K = 4127 shape repitches into it) and the split tail's epochs are shared.
+    # the library at the same time: plan caches, the table of per-stream
+    # workspaces (the K = 4127 shape repitches into its stream's) and the
+    # split tail's epochs are shared.
     import threading
     cases = [
         (96, 640, 4127, None), (256, 512, 1024, None), (32, 1024, 512, Options(path=PATH_DECODE)),
@@ -410,6 +411,30 @@ def test_concurrent_host_threads_on_separate_streams():
     for i, (_, _, _, _, ref) in enumerate(data):
         for r in range(6):
             compare(y_bits(outs[i][r]), ref, f"thread {i} call {r}")
+
+
+def test_unaligned_calls_allocate_nothing_once_the_stream_has_a_workspace():
+    # Calls whose rows are repitched and that bring no workspace use the one
+    # the device keeps for their stream: after a stream's first such call,
+    # its further calls allocate no device memory.  Two streams alternate.
+    M, N, K = 320, 528, 4127
+    x, w, s = synth.make_inputs(M, N, K, seed=31)
+    ref = oracle.linear(x, w, s)
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    assert fg.plan(M, N, K).repitch == 1
+    for i in range(2):
+        fg.fp8_gemm_scaled(xd, wd, sd, ys[i], streams[i])
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for i in range(2, 8):
+        fg.fp8_gemm_scaled(xd, wd, sd, ys[i], streams[i % 2])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    fg.check_device_error()
+    for i, y in enumerate(ys):
+        compare(y_bits(y), ref, f"stream workspace call {i}")
 
 
 # ------------------------------------------------------------------ bitwise pins
@@ -676,16 +701,19 @@ def test_entry_points_leave_the_current_device_unchanged():
 
 
 # ------------------------------------------------------------------ CUDA graph capture
-@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (512, 1024, 512), (32, 2048, 1024)])
+@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (512, 1024, 512), (32, 2048, 1024),
+                                   (300, 640, 4127), (32, 1024, 1001)])
 def test_cuda_graph_capture_and_replay_with_new_data(M, N, K):
-    # A call that needs no workspace enqueues only kernel launches, so it can
-    # be captured into a CUDA graph; a replay recomputes from whatever the
-    # captured buffers hold at that time (nothing is cached).
+    # A captured call becomes its kernel launches (plus, when its rows must
+    # be repitched, the workspace allocation and free as graph memory nodes);
+    # a replay recomputes from whatever the captured buffers hold at that
+    # time (nothing is cached).
     x1, w1, s1 = synth.make_inputs(M, N, K, seed=61)
     x2, w2, s2 = synth.make_inputs(M, N, K, seed=62)
     xd, wd, sd = to_dev(x1), to_dev(w1), to_dev(s1)
+    x_in = to_dev(x1)  # copied into xd inside the graph: a copy node precedes the first call
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    assert fg.plan(M, N, K).workspace_bytes == 0
+    assert (fg.plan(M, N, K).workspace_bytes == 0) == (K % 16 == 0)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -694,14 +722,15 @@ def test_cuda_graph_capture_and_replay_with_new_data(M, N, K):
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
+        xd.copy_(x_in)
         fg.fp8_gemm_scaled(xd, wd, sd, y)
-        fg.fp8_gemm_scaled(xd, wd, sd, y)  # two launches back to back in the graph
+        fg.fp8_gemm_scaled(xd, wd, sd, y)  # two calls back to back in the graph
     y.zero_()
     g.replay()
     torch.cuda.synchronize()
     fg.check_device_error()
     compare(y_bits(y), oracle.linear(x1, w1, s1), "graph replay 1")
-    xd.copy_(to_dev(x2))
+    x_in.copy_(to_dev(x2))
     wd.copy_(to_dev(w2))
     sd.copy_(to_dev(s2))
     g.replay()

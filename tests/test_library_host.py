@@ -54,8 +54,8 @@ def test_header_compiles_as_c():
 
 def test_version_and_status_strings(cdll):
     import fp8_channel_scaled_gb300 as f
-    assert f.fp8_gemm_version() == 3
-    for s in range(8):
+    assert f.fp8_gemm_version() == 4
+    for s in range(9):
         assert f.fp8_gemm_status_string(s) and f.fp8_gemm_status_string(s) != "unknown status"
     assert f.fp8_gemm_status_string(99) == "unknown status"
 
