@@ -232,7 +232,10 @@ size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M,
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current), which may load the
  * library's module; make that first call before any stream capture.
- * Arguments, layouts and error behaviour are those of fp8_gemm_scaled.
+ * Arguments and layouts are those of fp8_gemm_scaled, and so is the error
+ * behaviour, with two differences: a call whose workspace would exceed the
+ * array returns FP8GEMM_ESIZE (it never switches to the slow in-kernel
+ * loader on its own), and FP8GEMM_ENOMEM cannot occur.
  */
 #define FP8GEMM_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 int fp8_gemm_scaled_noalloc(const void *x, const void *w, const float *scale, void *y,
