@@ -77,8 +77,8 @@ struct DevState {
   // Occupancy of each kernel configuration, queried once on first use so that
   // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
   int tc2_pairs[6][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
-  int dec_blocks[3][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
-  int dec_clusters[3][6][2][9];  // ... [splits]: resident clusters
+  int dec_blocks[4][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
+  int dec_clusters[4][6][2][9];  // ... [splits]: resident clusters
   std::atomic<unsigned long long> calls{0};  // split-tail calls launched (epoch source)
 };
 
@@ -108,7 +108,7 @@ unsigned long long budget_ns() {
 const int kTcTiles[] = {256, 224, 192, 160, 128, 64};  // 64: one-CTA tiles only
 const int kTcStages[] = {3, 4, 5, 6, 7, 8, 9};
 const int kTc2Stages[] = {3, 4};
-const int kDecMp[] = {32, 64, 128};
+const int kDecMp[] = {32, 64, 128, 256};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
 // Makes device `dev` current for the guard's lifetime and makes the caller's
@@ -504,13 +504,6 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   const bool w_tma = (ldw % 16 == 0) && (!w || aligned16(w));
   const bool tma_ok = x_tma && w_tma;
   const bool contiguous = ldx == static_cast<size_t>(K) && ldw == static_cast<size_t>(K);
-  int path = o.path;
-  // M <= 64: the decode path.  Up to M = 128 it still wins while the weight
-  // is at most 64 n-tiles of 128 rows (measured at N = 4096: M = 96 10.2 vs
-  // 13.5 us, M = 128 11.1 vs 13.5 us; at N = 14336 the tile kernel is faster).
-  if (path == FP8GEMM_PATH_AUTO)
-    path = (M <= 64 || (M <= 128 && N <= 64 * 128)) ? FP8GEMM_PATH_DECODE : FP8GEMM_PATH_MAIN;
-  if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
   // Operands TMA cannot tile are repitched into a workspace first, unless the
   // caller forbids it or asks for the in-kernel loader.  (On the decode path
   // too: the in-kernel loader holds its loads in registers and cannot keep
@@ -521,6 +514,18 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   // K == 0 has nothing to load; the realigning variant then issues no copy
   // and needs no tensor map.
   const bool realign = !repitch && (o.force_realign != 0 || !tma_ok || K == 0);
+  int path = o.path;
+  // M <= 64: the decode path.  Up to M = 192 it still wins while the weight
+  // is at most 64 n-tiles of 128 rows (measured at N = 4096: M = 96 10.2 vs
+  // 13.5 us, M = 128 10.2 vs 12.9 us, M = 160 11.1 vs 13.1 us, M = 192 11.8
+  // vs 13.2 us; M = 256 13.2 vs 13.3 us; at N = 14336 the tile kernel is
+  // faster).  129-192 rows run the decode kernel with x padded to 256 rows,
+  // which is built for the TMA loader only.
+  if (path == FP8GEMM_PATH_AUTO)
+    path = (M <= 64 || (M <= 192 && N <= 64 * 128 && (M <= 128 || !realign)))
+               ? FP8GEMM_PATH_DECODE
+               : FP8GEMM_PATH_MAIN;
+  if (path != FP8GEMM_PATH_MAIN && path != FP8GEMM_PATH_DECODE) return FP8GEMM_EINVAL;
   if (realign && K > 0 && !contiguous) return FP8GEMM_EALIGN;  // in-kernel loader needs pitch K
   pl->pub.path = path;
   pl->pub.realign = realign ? 1 : 0;
@@ -568,9 +573,9 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   // streaming ceil(num_kb / s) K blocks.  How many clusters can be resident
   // at once is limited by cluster placement (CTAs of a cluster share a GPC),
   // not only by per-SM resources, so it is queried for each candidate.
-  if (M > 128) return FP8GEMM_EUNSUPPORTED;
+  if (M > 256) return FP8GEMM_EUNSUPPORTED;
   const int num_kb = (K + 127) / 128;
-  const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
+  const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   const int n_tiles = (N + 127) / 128;
   int best_s = 0, best_stages = 0, best_occ = 0;
   double best_cost = 1e300;

@@ -63,7 +63,7 @@ struct DCfg {
   static constexpr int kScaleOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
   static constexpr int kSmemBytes = 1024 + kScaleOff + kBN * 4;
   static constexpr int kTmemCols = tmem_cols_for<MP>();
-  static_assert(MP % 32 == 0 && MP >= 32 && MP <= 128, "MP");
+  static_assert(MP % 32 == 0 && MP >= 32 && MP <= 256, "MP");
 };
 
 template <int MP, int STAGES, bool REALIGN>
@@ -342,7 +342,8 @@ const DEntry kDEntries[] = {
     make_dentry<32, 6, false>(),  make_dentry<32, 8, false>(),  make_dentry<32, 10, false>(),
     make_dentry<64, 2, false>(),  make_dentry<64, 3, false>(),  make_dentry<64, 4, false>(),
     make_dentry<64, 6, false>(),  make_dentry<64, 8, false>(),  make_dentry<128, 2, false>(),
-    make_dentry<128, 4, false>(), make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),
+    make_dentry<128, 4, false>(), make_dentry<256, 2, false>(), make_dentry<256, 3, false>(),
+    make_dentry<256, 4, false>(), make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),
     make_dentry<64, 3, true>(),   make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
 };
 

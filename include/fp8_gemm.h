@@ -85,10 +85,11 @@ typedef enum {
 
 /* Kernel path. */
 enum {
-    FP8GEMM_PATH_AUTO = 0,    /* M <= 64, or M <= 128 with N <= 8192: decode path,
+    FP8GEMM_PATH_AUTO = 0,    /* M <= 64, or M <= 192 with N <= 8192: decode path,
                                  else main path */
     FP8GEMM_PATH_MAIN = 1,    /* persistent tcgen05 tile kernel */
-    FP8GEMM_PATH_DECODE = 2   /* split-K swap-AB kernel; needs M <= 128 */
+    FP8GEMM_PATH_DECODE = 2   /* split-K swap-AB kernel; needs M <= 256 (M > 128
+                                 only with 16-byte aligned rows or a workspace) */
 };
 
 /*

@@ -271,6 +271,7 @@ def test_split_tail_back_to_back_on_one_stream():
 DECODE_SHAPES = [
     (1, 128, 128), (5, 136, 256), (32, 1024, 2048), (33, 1000, 1000), (64, 384, 4096),
     (17, 257, 4127), (32, 128, 8192), (100, 256, 512), (2, 8, 16),
+    (129, 384, 1024), (200, 1000, 2048), (256, 640, 4096), (256, 136, 4127),
 ]
 
 
@@ -278,6 +279,21 @@ DECODE_SHAPES = [
 def test_decode_path_shapes(M, N, K):
     x, w, s = synth.make_inputs(M, N, K, seed=M + N + K)
     check_full(x, w, s, Options(path=PATH_DECODE), what=f"decode {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [150, 192])
+def test_mid_m_decode_path_and_its_no_workspace_fallback(M):
+    # 129-192 rows (N <= 8192) take the decode kernel with x padded to 256
+    # rows; that kernel has no realigning loader, so with no_workspace and
+    # unaligned rows the plan moves to the tile kernel's loader
+    N, K = 640, 4127
+    x, w, s = synth.make_inputs(M, N, K, seed=M)
+    p = fg.plan(M, N, K)
+    assert p.path == PATH_DECODE and p.tile_n == 256 and p.repitch == 1
+    check_full(x, w, s, what=f"mid-M {M} decode")
+    p2 = fg.plan(M, N, K, options=Options(no_workspace=True))
+    assert p2.path == PATH_MAIN and p2.realign == 1
+    check_full(x, w, s, Options(no_workspace=True), what=f"mid-M {M} no workspace")
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
