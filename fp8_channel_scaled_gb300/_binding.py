@@ -29,7 +29,8 @@ class _COptions(ctypes.Structure):
                 ("no_workspace", ctypes.c_int), ("mma_ctas", ctypes.c_int),
                 ("split_tail", ctypes.c_int), ("reserved", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("ldx", ctypes.c_size_t), ("ldw", ctypes.c_size_t)]
+                ("ldx", ctypes.c_size_t), ("ldw", ctypes.c_size_t),
+                ("epilogue_warps", ctypes.c_int)]
 
 
 _PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "grid", "cluster",
@@ -39,7 +40,7 @@ _PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "
 
 class _CPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in _PLAN_INT_FIELDS] + [
-        ("workspace_bytes", ctypes.c_size_t)]
+        ("workspace_bytes", ctypes.c_size_t), ("epilogue_warps", ctypes.c_int)]
 
 
 @dataclass
@@ -56,6 +57,7 @@ class Options:
     workspace_bytes: int = 0
     ldx: int = 0                # row pitch of x in bytes, 0 = K (set from strided views)
     ldw: int = 0                # row pitch of w in bytes, 0 = K
+    epilogue_warps: int = 0     # CTA-pair tiles: 0 auto, 4 or 8
 
     def _c(self) -> _COptions:
         o = _COptions()
@@ -67,6 +69,7 @@ class Options:
         o.workspace = int(self.workspace) or None
         o.workspace_bytes = int(self.workspace_bytes)
         o.ldx, o.ldw = int(self.ldx), int(self.ldw)
+        o.epilogue_warps = int(self.epilogue_warps)
         return o
 
 
@@ -88,6 +91,7 @@ class Plan:
     split_tiles: int
     tail_workers: int
     workspace_bytes: int
+    epilogue_warps: int = 4
 
 
 _lock = threading.RLock()
@@ -276,7 +280,8 @@ def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None =
     p = _CPlan()
     _check(lib().fp8_gemm_plan(int(device), x_ptr or None, w_ptr or None, int(M), int(N), int(K),
                                ctypes.byref(o), ctypes.byref(p)), "fp8_gemm_plan")
-    return Plan(*[getattr(p, f) for f in _PLAN_INT_FIELDS], int(p.workspace_bytes))
+    return Plan(*[getattr(p, f) for f in _PLAN_INT_FIELDS], int(p.workspace_bytes),
+                int(p.epilogue_warps))
 
 
 def fp8_gemm_workspace_bytes(device: int, M: int, N: int, K: int, options: Options | None = None,

@@ -76,7 +76,7 @@ struct DevState {
   int ws_count = 0;
   // Occupancy of each kernel configuration, queried once on first use so that
   // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
-  int tc2_pairs[6][2];           // [kTcTiles][kTc2Stages]: resident CTA pairs
+  int tc2_pairs[6][3][2];        // [kTcTiles][kTc2Stages][epilogue warps 4, 8]: resident pairs
   int dec_blocks[4][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
   int dec_clusters[4][6][2][9];  // ... [splits]: resident clusters
   std::atomic<unsigned long long> calls{0};  // split-tail calls launched (epoch source)
@@ -107,7 +107,10 @@ unsigned long long budget_ns() {
 
 const int kTcTiles[] = {256, 224, 192, 160, 128, 64};  // 64: one-CTA tiles only
 const int kTcStages[] = {3, 4, 5, 6, 7, 8, 9};
-const int kTc2Stages[] = {3, 4};
+const int kTc2Stages[] = {2, 3, 4};
+// Tiles of at most this many K blocks (K <= 1024) may take the pair kernel
+// with eight epilogue warps: there the epilogue, not the MMA, sets the pace.
+constexpr int kEpi8MaxKb = 8;
 const int kDecMp[] = {32, 64, 128, 256};
 const int kDecStages[] = {2, 3, 4, 6, 8, 10};
 
@@ -187,10 +190,11 @@ int device_state(int dev, DevState** out) {
   }
   for (int bn : kTcTiles)
     for (int s : kTc2Stages)
-      if (tc2_config_supported(bn, s) && tc2_prepare(bn, s) != cudaSuccess) {
-        cudaGetLastError();
-        return d.status;
-      }
+      for (int epi : {4, 8})
+        if (tc2_config_supported(bn, s, epi) && tc2_prepare(bn, s, epi) != cudaSuccess) {
+          cudaGetLastError();
+          return d.status;
+        }
   for (bool r : {false, true}) {
     for (int bn : kTcTiles)
       for (int s : kTcStages)
@@ -278,15 +282,15 @@ int index_of(const T (&arr)[n], T v) {
   return -1;
 }
 
-// Resident CTA pairs of the pair kernel (bn, stages) on the whole device.
-int tc2_pairs(DevState& d, int bn, int stages) {
+// Resident CTA pairs of the pair kernel (bn, stages, epi) on the whole device.
+int tc2_pairs(DevState& d, int bn, int stages, int epi) {
   const int i = index_of(kTcTiles, bn), j = index_of(kTc2Stages, stages);
-  if (i < 0 || j < 0) return 0;
+  if (i < 0 || j < 0 || (epi != 4 && epi != 8)) return 0;
   std::lock_guard<std::mutex> lk(g_mu);
-  int& v = d.tc2_pairs[i][j];
+  int& v = d.tc2_pairs[i][j][epi == 8 ? 1 : 0];
   if (v < 0) {
     int pairs = 0;
-    if (tc2_max_active_pairs(bn, stages, d.sm_count & ~1, &pairs) != cudaSuccess) {
+    if (tc2_max_active_pairs(bn, stages, epi, d.sm_count & ~1, &pairs) != cudaSuccess) {
       cudaGetLastError();
       pairs = 0;
     }
@@ -440,12 +444,28 @@ int choose_tc(DevState& d, int M, int N, int num_kb, bool realign, bool can_spli
       if (o.tile_n && bn != o.tile_n) continue;
       int stages, units;
       if (ctas == 2) {
-        stages = o.stages ? o.stages : tc2_max_stages(bn, d.smem_optin);
-        if (stages == 0 || !tc2_config_supported(bn, stages) ||
-            tc2_smem_bytes(bn, stages) > d.smem_optin)
-          continue;
+        if (o.epilogue_warps != 0 && o.epilogue_warps != 4 && o.epilogue_warps != 8)
+          return FP8GEMM_EINVAL;
         const long long tiles = static_cast<long long>((M + 255) / 256) * ((N + bn - 1) / bn);
-        const int pairs = tc2_pairs(d, bn, stages);
+        // Eight epilogue warps for short-K tiles when every pair has at least
+        // two tiles, so that epilogues overlap mainloops (8192 x 8192 x 128:
+        // 64.5 -> 54.6 us, x 1024: 73.0 -> 67.4 us; with K = 2048 the two-stage
+        // ring they leave room for is slower, 87.8 -> 104.8 us; one tile per
+        // pair, 512 x 4096 x 1024: 8.3 -> 8.7 us).  No split tail with them.
+        int epi = o.epilogue_warps;
+        if (epi == 0) {
+          const int pairs4 = tc2_pairs(d, bn, tc2_max_stages(bn, d.smem_optin, 4), 4);
+          epi = (num_kb <= kEpi8MaxKb && !can_split && pairs4 > 0 && tiles >= 2LL * pairs4 &&
+                 tc2_max_stages(bn, d.smem_optin, 8) > 0)
+                    ? 8
+                    : 4;
+        }
+        if (epi == 8 && (can_split || num_kb > 24)) continue;
+        stages = o.stages ? o.stages : tc2_max_stages(bn, d.smem_optin, epi);
+        if (stages == 0 || !tc2_config_supported(bn, stages, epi) ||
+            tc2_smem_bytes(bn, stages, epi) > d.smem_optin)
+          continue;
+        const int pairs = tc2_pairs(d, bn, stages, epi);
         if (pairs <= 0) continue;
         // with a split tail the last wave costs its share of the tail's K
         // blocks plus the owners' reads of the other segments' partial sums
@@ -463,7 +483,7 @@ int choose_tc(DevState& d, int M, int N, int num_kb, bool realign, bool can_spli
         const double cost = waves * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
         if (cost < best - 1e-9) {
           best = cost;
-          pick = TcConfig{2, bn, stages, false, 2 * units, 16, tw};
+          pick = TcConfig{2, bn, stages, false, 2 * units, 16, tw, epi};
         }
       } else {
         stages = o.stages ? o.stages : tc_max_stages(bn, realign, d.smem_optin);
@@ -477,7 +497,7 @@ int choose_tc(DevState& d, int M, int N, int num_kb, bool realign, bool can_spli
             1.3 * static_cast<double>(waves) * bn * (1.0 + 0.15 * (256 - bn) / 128.0);
         if (cost < best - 1e-9) {
           best = cost;
-          pick = TcConfig{1, bn, stages, realign, units, 16, 0};
+          pick = TcConfig{1, bn, stages, realign, units, 16, 0, 4};
         }
       }
     }
@@ -562,8 +582,9 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
     pl->pub.splits = 1;
     pl->pub.grid = pl->tc.grid;
     pl->pub.cluster = pair ? 2 : 1;
-    pl->pub.threads = pair ? tc2_threads() : tc_threads(realign);
-    pl->pub.smem_bytes = pair ? tc2_smem_bytes(pl->tc.bn, pl->tc.stages)
+    pl->pub.threads = pair ? tc2_threads(pl->tc.epi) : tc_threads(realign);
+    pl->pub.epilogue_warps = pair ? pl->tc.epi : 4;
+    pl->pub.smem_bytes = pair ? tc2_smem_bytes(pl->tc.bn, pl->tc.stages, pl->tc.epi)
                               : tc_smem_bytes(pl->tc.bn, pl->tc.stages, realign);
     pl->pub.occupancy = 1;  // one CTA per SM: the ring fills shared memory
     return FP8GEMM_OK;
@@ -993,7 +1014,7 @@ extern "C" int fp8_gemm_grouped(const void* x, const void* w, const float* scale
   st = make_plan(*d, x, w, M, N, K, &o, &pl);
   if (st != FP8GEMM_OK) return st;
   if (pl.pub.realign || pl.pub.repitch) return FP8GEMM_EALIGN;
-  const int pairs = tc2_pairs(*d, pl.tc.bn, pl.tc.stages);
+  const int pairs = tc2_pairs(*d, pl.tc.bn, pl.tc.stages, pl.tc.epi);
   if (pairs <= 0) return FP8GEMM_ELAUNCH;
   pl.tc.grid = 2 * pairs;
   pl.tc.tail_workers = 0;

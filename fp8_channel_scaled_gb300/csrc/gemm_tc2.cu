@@ -41,17 +41,28 @@ namespace fp8g {
 namespace {
 
 constexpr int kBK = 128;
-constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;   // warps 5-8: x first half, x second half, w first, w second
 constexpr int kKbPerStage = 2;  // 128-byte K blocks per pipeline stage
-constexpr int kThreads = 288;
 constexpr int kStgBytes = 2048;  // one 32 x 32 bf16 staging box (64-byte swizzle)
 // tiles of at most this many K blocks (K <= 3072) take the rolled epilogue loop
 constexpr int kRolledEpilogueMaxKb = 24;
 
-template <int BN, int STAGES>
+// EPI epilogue warps (4, or 8 for short-K tiles where the epilogue, not the
+// MMA, sets the pace: two warps per TMEM lane quarter, each storing half of
+// the tile's columns), then the TMEM/MMA warp, then the TMA producer warps
+// (x first K block, x second, w first, w second; w's two by one warp when
+// there are eight epilogue warps).
+template <int BN, int STAGES, int EPI = 4>
 struct Cfg2 {
+  static constexpr int kEpiWarps = EPI;
+  static constexpr int kMmaWarp = EPI;
+  static constexpr int kProdWarp0 = EPI + 1;
+  // four TMA producer warps, or three with eight epilogue warps (the third
+  // issues both of w's K blocks): twelve warps leave 168 registers a thread
+  static constexpr int kNumProd = EPI == 8 ? 3 : 4;
+  static constexpr int kThreads = 32 * (EPI + 1 + kNumProd);
+  static constexpr int kChunks = BN / 32;
+  // chunks [0, kSplit) belong to warps 0-3, [kSplit, kChunks) to warps 4-7
+  static constexpr int kSplit = EPI == 8 ? (kChunks + 1) / 2 : kChunks;
   static constexpr int kABytes1 = 128 * kBK;       // this CTA's 128 rows of x, one K block
   static constexpr int kBRows = BN / 2;            // this CTA's rows of w
   static constexpr int kBBytes1 = kBRows * kBK;    // ... one K block
@@ -59,7 +70,7 @@ struct Cfg2 {
   static constexpr int kBBytes = kKbPerStage * kBBytes1;
   static constexpr int kStageBytes = kABytes + kBBytes;  // [x kb0][x kb1][w kb0][w kb1]
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
-  static constexpr int kStgOff = STAGES * kStageBytes;            // 4 warps x 2 staging boxes
+  static constexpr int kStgOff = STAGES * kStageBytes;            // EPI warps x 2 staging boxes
   static constexpr int kNumBars = 2 * STAGES + 6 + kEpiWarps;  // + one per epilogue warp
   // each epilogue warp's copy of the tile's BN scales, where it fits
   static constexpr int kScOff = kStgOff + kEpiWarps * 2 * kStgBytes;
@@ -68,17 +79,20 @@ struct Cfg2 {
   static constexpr int kBarOff = kScOff + (kScInSmem ? kEpiWarps * BN * 4 : 0);
   static constexpr int kPartBytes = BN * 128;  // one warp's share of a partial sum (32 x BN fp32)
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  static_assert(EPI == 4 || EPI == 8, "epilogue warps");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(kBRows % 8 == 0, "B half must be whole 8-row swizzle atoms");
   static_assert(kKbPerStage == 1 || kKbPerStage == 2, "K blocks per stage");
   static_assert(kKbPerStage == 2 || STAGES % 2 == 0, "one-K-block stages alternate producers");
   static_assert(kABytes1 % 1024 == 0 && kBBytes1 % 1024 == 0,
                 "every K block of a stage must start on a 1024-byte swizzle atom");
-  static_assert(kEpiWarps * kPartBytes <= STAGES * kStageBytes,
+  // the split tail and the last unit shared with the producers exist with
+  // four epilogue warps only
+  static_assert(EPI == 8 || kEpiWarps * kPartBytes <= STAGES * kStageBytes,
                 "a partial sum must fit in the ring it reuses");
   // last unit: 8 warps x (up to) half the chunks, one staging box each
   static constexpr int kHalf = (BN / 32 + 1) / 2;
-  static_assert(2 * kEpiWarps * kHalf * kStgBytes <= STAGES * kStageBytes,
+  static_assert(EPI == 8 || 2 * kEpiWarps * kHalf * kStgBytes <= STAGES * kStageBytes,
                 "the last unit's staging boxes must fit in the ring");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -178,13 +192,17 @@ __device__ __forceinline__ void store_chunks(uint32_t t_row, uint32_t stg,
 // ROLLED: the owner epilogue's chunk loop is rolled (two chunks per
 // iteration) instead of fully unrolled; chosen for tiles of at most
 // kRolledEpilogueMaxKb K blocks (see the loop).
-template <int BN, int STAGES, bool ROLLED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, bool ROLLED, int EPI>
+__global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
     fp8_linear_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmY, const GemmArgs p,
                           const int num_m2_blk, const int num_n_blk, const int group_m) {
-  using C = Cfg2<BN, STAGES>;
+  using C = Cfg2<BN, STAGES, EPI>;
+  static_assert(EPI == 4 || ROLLED, "eight epilogue warps use the rolled loop");
+  constexpr int kEpiWarps = C::kEpiWarps;
+  constexpr int kMmaWarp = C::kMmaWarp;
+  constexpr int kProdWarp0 = C::kProdWarp0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -280,9 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q = warp - kProdWarp0;
       const bool is_a = q < 2;
       // two K blocks per stage: this thread loads K block `sub` of every
-      // stage; one: it loads every other stage (those with it % 2 == sub)
+      // stage; one: it loads every other stage (those with it % 2 == sub).
+      // With three producer warps the third loads both of w's K blocks.
       const int sub = static_cast<int>(q & 1u);
       const int half = kKbPerStage == 2 ? sub : 0;
+      const int n_halves = (C::kNumProd == 3 && !is_a) ? 2 : 1;
       const CUtensorMap* map = is_a ? &tmA : &tmB;
       const uint32_t bytes = is_a ? C::kABytes1 : C::kBBytes1;
       const uint32_t off = is_a ? static_cast<uint32_t>(half * C::kABytes1)
@@ -304,12 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (kb + half < wu.k1) {
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
-            tma_load_2d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) + off, map,
-                             mapa_shared(full_bar(stage), 0u), (kb + half) * kBK, row);
-          } else if (rank == 0) {
-            mbar_arrive(full_bar(stage));  // odd K-block count: this half stays empty
+          for (int hh = 0; hh < n_halves; ++hh) {
+            const int h = half + hh;
+            const uint32_t o = off + static_cast<uint32_t>(hh) * bytes;
+            if (kb + h < wu.k1) {
+              if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+              tma_load_2d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) + o, map,
+                               mapa_shared(full_bar(stage), 0u), (kb + h) * kBK, row);
+            } else if (rank == 0) {
+              mbar_arrive(full_bar(stage));  // odd K-block count: this half stays empty
+            }
           }
         }
       }
@@ -345,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lu = u;
         ++n_units;
       }
-      if (n_units > 0 && lu.owner && lu.q_end == pair + 1 && p.vec_store) {
+      if (EPI == 4 && n_units > 0 && lu.owner && lu.q_end == pair + 1 && p.vec_store) {
         // the epilogue warps arrive once they have seen the last accumulator
         // complete (a parity wait on tfull itself could not tell its uses apart)
         if (mbar_wait_bounded(last_bar, 0u, wc, kErrWaitEpilogue)) {
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t stg = sbase + (kEpiWarps + (warp - kProdWarp0)) * C::kHalf * kStgBytes;
           // the scales were staged by epilogue warp `quarter` before it
           // arrived on last_bar
-          store_chunks<BN, C::kHalf, BN / 32>(t_row, stg, &tmY, p, row0, tg.row_end, tg.nb,
+          store_chunks<BN, C::kHalf, C::kChunks>(t_row, stg, &tmY, p, row0, tg.row_end, tg.nb,
                                               tg.sbase, lane, num_kb == 0,
                                               C::kScInSmem ? sc_of(quarter) : nullptr);
           if (lane == 0) tma_store_wait_read<0>();
@@ -423,6 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool tma_y = p.vec_store != 0;
     const uint32_t stg = sbase + static_cast<uint32_t>(C::kStgOff) + warp * 2u * kStgBytes;
     constexpr int kChunks = BN / 32;
+    // TMEM lane quarter (= tile rows) and chunk range of this warp: all
+    // chunks of its quarter with four epilogue warps, half of them with eight
+    const uint32_t quarter = warp & 3u;
+    const int c_lo = warp < 4u ? 0 : C::kSplit;
+    const int c_hi = warp < 4u ? C::kSplit : kChunks;
     // This warp's share of worker q's published partial sum: 32 rows x BN
     // columns stored [chunk][column][row], so that each store and load
     // instruction of the warp covers 128 contiguous bytes.
@@ -440,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool last = !peek.next(nxt);
       const TileGeom tg = tm.at(wu.tile);
       const int nb = tg.nb;
-      const int row0 = tg.row + static_cast<int>(rank) * 128 + static_cast<int>(warp) * 32;
+      const int row0 = tg.row + static_cast<int>(rank) * 128 + static_cast<int>(quarter) * 32;
       const int row = row0 + static_cast<int>(lane);
-      const uint32_t t_row = tmem_base + ((warp * 32u) << 16) + acc * BN;
+      const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * BN;
       // TMEM -> registers double buffered: chunk c+1 is in flight while chunk c
       // is used (its registers are read only after the next tcgen05.wait::ld)
       uint32_t va[32], vb[32];
@@ -463,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       };
-      if (last && wu.owner && wu.q_end == pair + 1 && tma_y) {
+      if (EPI == 4 && last && wu.owner && wu.q_end == pair + 1 && tma_y) {
         // ---- the last unit, shared with the producer warps (see there): the
         // operand ring is idle, each chunk gets its own staging box in it
         if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, wc, kErrWaitEpilogue)) break;
@@ -591,17 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Chunks are handled in pairs (va, vb ping-pong): both are
           // computed, then staged in the warp's two boxes once the previous
           // pair's stores have read them, with one proxy fence for the two.
-          tmem_ld_32x32b_x32(t_row, va);
+          tmem_ld_32x32b_x32(t_row + c_lo * 32, va);
 #pragma unroll 1
-          for (int c = 0; c < kChunks; c += 2) {
-            const bool two = c + 1 < kChunks;
+          for (int c = c_lo; c < c_hi; c += 2) {
+            const bool two = c + 1 < c_hi;
             uint32_t pk0[16], pk1[16];
             tmem_ld_wait();
             if (two) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
             compute(c, va, pk0);
             if (two) {
               tmem_ld_wait();
-              if (c + 2 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
+              if (c + 2 < c_hi) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
               compute(c + 1, vb, pk1);
             }
             if (tma_y) {
@@ -714,50 +743,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ dispatch
 struct Entry2 {
-  int bn, stages;
-  const void* fn;         // unrolled owner epilogue loop
+  int bn, stages, epi;
+  const void* fn;         // unrolled owner epilogue loop (four epilogue warps only)
   const void* fn_rolled;  // rolled loop, for tiles of at most kRolledEpilogueMaxKb K blocks
-  int smem;
+  int smem, threads;
 };
 
 template <int BN, int S>
 Entry2 make_entry2() {
-  return Entry2{BN, S, reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, false>),
-                reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, true>),
-                Cfg2<BN, S>::kSmemBytes};
+  return Entry2{BN, S, 4, reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, false, 4>),
+                reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, true, 4>),
+                Cfg2<BN, S, 4>::kSmemBytes, Cfg2<BN, S, 4>::kThreads};
+}
+
+// Eight epilogue warps: rolled loop only, for short-K tiles.
+template <int BN, int S>
+Entry2 make_entry8() {
+  const void* f = reinterpret_cast<const void*>(&fp8_linear_tc2_kernel<BN, S, true, 8>);
+  return Entry2{BN, S, 8, f, f, Cfg2<BN, S, 8>::kSmemBytes, Cfg2<BN, S, 8>::kThreads};
 }
 
 const Entry2 kEntries2[] = {
     make_entry2<256, 3>(), make_entry2<224, 3>(), make_entry2<192, 3>(), make_entry2<160, 4>(),
-    make_entry2<128, 4>(),
+    make_entry2<128, 4>(), make_entry8<256, 2>(), make_entry8<224, 3>(), make_entry8<192, 3>(),
+    make_entry8<160, 3>(), make_entry8<128, 3>(),
 };
 
-const Entry2* find2(int bn, int stages) {
+const Entry2* find2(int bn, int stages, int epi) {
   for (const Entry2& e : kEntries2)
-    if (e.bn == bn && e.stages == stages) return &e;
+    if (e.bn == bn && e.stages == stages && e.epi == epi) return &e;
   return nullptr;
 }
 
 }  // namespace
 
-bool tc2_config_supported(int bn, int stages) { return find2(bn, stages) != nullptr; }
+bool tc2_config_supported(int bn, int stages, int epi) {
+  return find2(bn, stages, epi) != nullptr;
+}
 
-int tc2_smem_bytes(int bn, int stages) {
-  const Entry2* e = find2(bn, stages);
+int tc2_smem_bytes(int bn, int stages, int epi) {
+  const Entry2* e = find2(bn, stages, epi);
   return e ? e->smem : -1;
 }
 
-int tc2_threads() { return kThreads; }
+int tc2_threads(int epi) { return epi == 8 ? 32 * 12 : 32 * 9; }
 
-int tc2_max_stages(int bn, int smem_optin) {
+int tc2_max_stages(int bn, int smem_optin, int epi) {
   int best = 0;
   for (const Entry2& e : kEntries2)
-    if (e.bn == bn && e.smem <= smem_optin && e.stages > best) best = e.stages;
+    if (e.bn == bn && e.epi == epi && e.smem <= smem_optin && e.stages > best) best = e.stages;
   return best;
 }
 
-cudaError_t tc2_prepare(int bn, int stages) {
-  const Entry2* e = find2(bn, stages);
+cudaError_t tc2_prepare(int bn, int stages, int epi) {
+  const Entry2* e = find2(bn, stages, epi);
   if (!e) return cudaErrorInvalidValue;
   const cudaError_t r =
       cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
@@ -765,12 +804,12 @@ cudaError_t tc2_prepare(int bn, int stages) {
   return cudaFuncSetAttribute(e->fn_rolled, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
 }
 
-cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out) {
-  const Entry2* e = find2(bn, stages);
+cudaError_t tc2_max_active_pairs(int bn, int stages, int epi, int grid, int* out) {
+  const Entry2* e = find2(bn, stages, epi);
   if (!e) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(e->threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -779,18 +818,20 @@ cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, e->fn, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, e->fn_rolled, &cfg);
 }
 
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                        const GemmArgs& a, const TcConfig& c, cudaStream_t s) {
-  const Entry2* e = find2(c.bn, c.stages);
+  const Entry2* e = find2(c.bn, c.stages, c.epi);
   if (!e || c.grid % 2) return cudaErrorInvalidValue;
+  if (c.epi == 8 && (a.tail_workers > 0 || a.num_kb > kRolledEpilogueMaxKb))
+    return cudaErrorInvalidValue;  // no split tail and no unrolled loop with eight warps
   const int num_m2 = (a.M + 255) / 256;
   const int num_n = (a.N + c.bn - 1) / c.bn;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c.grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(e->threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(e->smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -48,6 +48,7 @@ struct TcConfig {
   int grid;        // persistent CTAs
   int group_m;     // M tiles per raster group
   int tail_workers;  // CTA pairs sharing the split tail (0: no split; pair kernel only)
+  int epi;         // pair kernel: epilogue warps, 4 or 8 (8: short-K tiles, no split tail)
 };
 bool tc_config_supported(int bn, int stages, bool realign);
 int tc_smem_bytes(int bn, int stages, bool realign);
@@ -59,12 +60,12 @@ cudaError_t launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
                       const TcConfig& c, cudaStream_t s);
 
 // ---- persistent tcgen05 kernel on CTA pairs (large M) -----------------------
-bool tc2_config_supported(int bn, int stages);
-int tc2_smem_bytes(int bn, int stages);
-int tc2_threads();
-int tc2_max_stages(int bn, int smem_optin);
-cudaError_t tc2_prepare(int bn, int stages);
-cudaError_t tc2_max_active_pairs(int bn, int stages, int grid, int* out);
+bool tc2_config_supported(int bn, int stages, int epi);
+int tc2_smem_bytes(int bn, int stages, int epi);
+int tc2_threads(int epi);
+int tc2_max_stages(int bn, int smem_optin, int epi);
+cudaError_t tc2_prepare(int bn, int stages, int epi);
+cudaError_t tc2_max_active_pairs(int bn, int stages, int epi, int grid, int* out);
 cudaError_t launch_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                        const GemmArgs& a, const TcConfig& c, cudaStream_t s);
 

@@ -68,7 +68,7 @@ extern "C" {
  * (identical to cudaStream_t). */
 typedef struct CUstream_st *fp8gemm_stream_t;
 
-#define FP8GEMM_VERSION 4
+#define FP8GEMM_VERSION 5
 
 typedef enum {
     FP8GEMM_OK = 0,
@@ -123,6 +123,9 @@ typedef struct {
                            place by TMA whatever K is (bytes past K in a row are never
                            read); any other operand is repitched into the workspace
                            (or, with pitch == K, loaded by the realigning producer) */
+    int epilogue_warps; /* CTA-pair tiles: 0 auto (8 when K <= 1024, every pair
+                           has at least two tiles and there is no split tail,
+                           else 4), 4, or 8 (K <= 3072, no split tail) */
 } fp8gemm_options;
 
 /* What a call with the same arguments would launch (see fp8_gemm_plan). */
@@ -147,6 +150,7 @@ typedef struct {
     int tail_workers;   /* CTA pairs sharing them; each publishes at most one
                            fp32 partial sum that the tile's owner adds */
     size_t workspace_bytes; /* device workspace the call needs (0 = none) */
+    int epilogue_warps; /* warps scaling and storing y per CTA (4 or 8) */
 } fp8gemm_plan;
 
 /*

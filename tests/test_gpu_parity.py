@@ -129,6 +129,33 @@ def test_cta_pair_equals_single_cta_on_exact_sums():
     assert np.array_equal(a, oracle.linear(x, w, s))
 
 
+@pytest.mark.parametrize("M,N,K,bn", [
+    (512, 1024, 128, 256), (300, 520, 256, 224), (1000, 2000, 1000, 0), (256, 777, 384, 192),
+    (768, 640, 3072, 128), (2048, 4096, 3001, 0), (600, 900, 700, 160),
+])
+def test_eight_epilogue_warps_match_four_bitwise(M, N, K, bn):
+    # Pair tiles whose epilogue is split over eight warps (two per TMEM lane
+    # quarter, each half the columns) store exactly what four warps store
+    x, w, s = synth.make_inputs(M, N, K, seed=M + K)
+    o8 = Options(path=PATH_MAIN, mma_ctas=2, tile_n=bn, epilogue_warps=8)
+    o4 = Options(path=PATH_MAIN, mma_ctas=2, tile_n=bn, epilogue_warps=4)
+    p8 = fg.plan(M, N, K, options=o8)
+    assert p8.epilogue_warps == 8 and p8.threads == 384
+    y8 = run(x, w, s, o8)
+    compare(y8, oracle.linear(x, w, s), f"eight epilogue warps {M}x{N}x{K}")
+    assert np.array_equal(y8, run(x, w, s, o4))
+
+
+def test_short_k_plans_take_eight_epilogue_warps():
+    assert fg.plan(8192, 8192, 128).epilogue_warps == 8
+    assert fg.plan(8192, 8192, 1024).epilogue_warps == 8
+    assert fg.plan(4096, 4096, 4096).epilogue_warps == 4
+    assert fg.plan(512, 4096, 1024).epilogue_warps == 4  # one tile per pair
+    assert fg.plan(4096, 4096, 1024, options=Options(split_tail=True)).epilogue_warps == 4
+    with pytest.raises(fg.FP8GemmError):
+        fg.plan(4096, 4096, 1024, options=Options(mma_ctas=2, epilogue_warps=6))
+
+
 @pytest.mark.parametrize("bn", [128, 224, 256])
 def test_main_path_realigning_loader(bn):
     x, w, s = synth.make_inputs(300, 520, 640, seed=5)
