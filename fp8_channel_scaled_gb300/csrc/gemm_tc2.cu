@@ -318,6 +318,15 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
                              : tg.wrow + static_cast<int>(rank) * C::kBRows;
         for (int kb = wu.k0; kb < wu.k1; kb += kKbPerStage, ++it) {
           if (kKbPerStage == 1 && static_cast<int>(it & 1u) != sub) continue;
+          // An odd CTA's producer whose K block of this stage lies past the
+          // unit's end (an odd number of K blocks) has nothing to load and
+          // must not wait for the stage either: the MMA does not need it
+          // there, so the stage could be released once more before the
+          // producer looks, and a parity wait cannot tell those two phases
+          // apart (it would wait for a completion that never comes).  The
+          // even CTA's producer still arrives on the full barrier, which the
+          // MMA waits for, so it can never fall that far behind.
+          if (rank != 0 && kb + half >= wu.k1) continue;
           const uint32_t stage = it % STAGES;
           const uint32_t use = it / STAGES;
           if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) {

@@ -481,6 +481,30 @@ def test_unaligned_calls_allocate_nothing_once_the_stream_has_a_workspace():
 
 
 # ------------------------------------------------------------------ bitwise pins
+@pytest.mark.parametrize("K", [4224, 4127, 1025])
+def test_pair_tiles_with_odd_k_block_counts_many_calls(K):
+    # With an odd number of K blocks the last stage of every tile holds one
+    # K block: the odd CTA's producer of the second one has nothing to load
+    # and must not wait for that stage (a stage released twice before it
+    # looks is indistinguishable to a parity wait).  Hundreds of consecutive
+    # calls of 2 tiles per CTA pair (33 or 9 K blocks, repitched or not)
+    # must all finish without a wait running out and give identical bits.
+    M, N = 2048, 4096
+    x, w, s = synth.make_inputs(M, N, K, seed=K)
+    xd, wd, sd = to_dev(x), to_dev(w), to_dev(s)
+    p = fg.plan(M, N, K)
+    assert p.cluster == 2 and ((K + 127) // 128) % 2 == 1
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for i in range(300):
+        fg.fp8_gemm_scaled(xd, wd, sd, ys[i % 3])
+    fg.check_device_error()
+    first = y_bits(ys[0])
+    rows = np.array([0, 1, 1023, M - 1])
+    compare(first[rows], oracle.linear_rows(x, w, s, rows), f"odd K blocks, K={K}")
+    for y in ys[1:]:
+        assert np.array_equal(y_bits(y), first)
+
+
 @pytest.mark.parametrize("path", [PATH_MAIN, PATH_DECODE])
 def test_one_hot_weights_reproduce_x_bitwise(path):
     M = 64 if path == PATH_DECODE else 192
