@@ -40,7 +40,8 @@ _PLAN_INT_FIELDS = ("path", "realign", "tile_m", "tile_n", "stages", "splits", "
 
 class _CPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in _PLAN_INT_FIELDS] + [
-        ("workspace_bytes", ctypes.c_size_t), ("epilogue_warps", ctypes.c_int)]
+        ("workspace_bytes", ctypes.c_size_t), ("epilogue_warps", ctypes.c_int),
+        ("kblocks_per_stage", ctypes.c_int)]
 
 
 @dataclass
@@ -92,6 +93,7 @@ class Plan:
     tail_workers: int
     workspace_bytes: int
     epilogue_warps: int = 4
+    kblocks_per_stage: int = 1
 
 
 _lock = threading.RLock()
@@ -281,7 +283,7 @@ def fp8_gemm_plan(device: int, M: int, N: int, K: int, options: Options | None =
     _check(lib().fp8_gemm_plan(int(device), x_ptr or None, w_ptr or None, int(M), int(N), int(K),
                                ctypes.byref(o), ctypes.byref(p)), "fp8_gemm_plan")
     return Plan(*[getattr(p, f) for f in _PLAN_INT_FIELDS], int(p.workspace_bytes),
-                int(p.epilogue_warps))
+                int(p.epilogue_warps), int(p.kblocks_per_stage))
 
 
 def fp8_gemm_workspace_bytes(device: int, M: int, N: int, K: int, options: Options | None = None,

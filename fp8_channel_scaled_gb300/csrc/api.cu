@@ -77,8 +77,8 @@ struct DevState {
   // Occupancy of each kernel configuration, queried once on first use so that
   // planning a call is plain arithmetic (-1: not queried yet, 0: cannot run).
   int tc2_pairs[6][3][2];        // [kTcTiles][kTc2Stages][epilogue warps 4, 8]: resident pairs
-  int dec_blocks[4][6][2];       // [kDecMp][kDecStages][realign]: CTAs per SM
-  int dec_clusters[4][6][2][9];  // ... [splits]: resident clusters
+  int dec_blocks[4][7][2][3];       // [kDecMp][kDecStages][realign][kDecKbs]: CTAs per SM
+  int dec_clusters[4][7][2][3][9];  // ... [splits]: resident clusters
   std::atomic<unsigned long long> calls{0};  // split-tail calls launched (epoch source)
 };
 
@@ -112,7 +112,8 @@ const int kTc2Stages[] = {2, 3, 4};
 // with eight epilogue warps: there the epilogue, not the MMA, sets the pace.
 constexpr int kEpi8MaxKb = 8;
 const int kDecMp[] = {32, 64, 128, 256};
-const int kDecStages[] = {2, 3, 4, 6, 8, 10};
+const int kDecStages[] = {2, 3, 4, 5, 6, 8, 10};
+const int kDecKbs[] = {1, 2, 4};  // 128-byte K blocks per decode stage
 
 // Makes device `dev` current for the guard's lifetime and makes the caller's
 // current device current again when it ends, so that no entry point leaves a
@@ -204,10 +205,11 @@ int device_state(int dev, DevState** out) {
         }
     for (int mp : kDecMp)
       for (int s : kDecStages)
-        if (dec_config_supported(mp, s, r) && dec_prepare(mp, s, r) != cudaSuccess) {
-          cudaGetLastError();
-          return d.status;
-        }
+        for (int kbs : kDecKbs)
+          if (dec_config_supported(mp, s, r, kbs) && dec_prepare(mp, s, r, kbs) != cudaSuccess) {
+            cudaGetLastError();
+            return d.status;
+          }
   }
   d.status = FP8GEMM_OK;
   return d.status;
@@ -302,17 +304,17 @@ int tc2_pairs(DevState& d, int bn, int stages, int epi) {
 // Resident decode CTAs per SM, or 0 if the configuration cannot run.  The
 // tensor-memory budget (512 columns per SM) must cover every resident CTA, or
 // a CTA's allocation would wait for another CTA to finish.
-int dec_occupancy(DevState& d, int mp, int stages, bool realign) {
-  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages);
-  if (i < 0 || j < 0) return 0;
+int dec_occupancy(DevState& d, int mp, int stages, bool realign, int kbs) {
+  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages), k = index_of(kDecKbs, kbs);
+  if (i < 0 || j < 0 || k < 0) return 0;
   std::lock_guard<std::mutex> lk(g_mu);
-  int& v = d.dec_blocks[i][j][realign ? 1 : 0];
+  int& v = d.dec_blocks[i][j][realign ? 1 : 0][k];
   if (v < 0) {
     v = 0;
-    const int smem = dec_smem_bytes(mp, stages, realign);
+    const int smem = dec_smem_bytes(mp, stages, realign, kbs);
     int blocks = 0;
     if (smem >= 0 && smem <= d.smem_optin) {
-      if (dec_blocks_per_sm(mp, stages, realign, &blocks) != cudaSuccess) {
+      if (dec_blocks_per_sm(mp, stages, realign, kbs, &blocks) != cudaSuccess) {
         cudaGetLastError();
         blocks = 0;
       }
@@ -325,14 +327,15 @@ int dec_occupancy(DevState& d, int mp, int stages, bool realign) {
 // Resident clusters of `splits` decode CTAs on the whole device.  Cluster
 // placement (the CTAs of a cluster share a GPC) limits this below the per-SM
 // count.  The query uses a grid large enough not to cap the answer.
-int dec_clusters(DevState& d, int mp, int stages, bool realign, int splits) {
-  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages);
-  if (i < 0 || j < 0 || splits < 1 || splits > 8) return 0;
+int dec_clusters(DevState& d, int mp, int stages, bool realign, int kbs, int splits) {
+  const int i = index_of(kDecMp, mp), j = index_of(kDecStages, stages), k = index_of(kDecKbs, kbs);
+  if (i < 0 || j < 0 || k < 0 || splits < 1 || splits > 8) return 0;
   std::lock_guard<std::mutex> lk(g_mu);
-  int& v = d.dec_clusters[i][j][realign ? 1 : 0][splits];
+  int& v = d.dec_clusters[i][j][realign ? 1 : 0][k][splits];
   if (v < 0) {
     int c = 0;
-    if (dec_max_active_clusters(mp, stages, realign, splits, splits * 1024, &c) != cudaSuccess) {
+    if (dec_max_active_clusters(mp, stages, realign, kbs, splits, splits * 1024, &c) !=
+        cudaSuccess) {
       cudaGetLastError();
       c = 0;
     }
@@ -351,6 +354,25 @@ int encode_operand(CUtensorMap* map, const void* base, int rows, int K, size_t p
   const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8GEMM_OK : FP8GEMM_ELAUNCH;
+}
+
+// TMA descriptor of the same byte matrix viewed as [K / 128 blocks][rows][128
+// bytes] (rows `pitch` bytes apart, K blocks 128 bytes apart; needs K % 128
+// == 0 so that the view of each row ends at its last byte), with boxes of
+// kbs K blocks x box_rows rows x 128 bytes and the 128-byte swizzle: one box
+// lands as kbs consecutive K-major tiles of box_rows x 128 bytes.  Rows past
+// `rows` read as zero.
+int encode_operand_kblocks(CUtensorMap* map, const void* base, int rows, int K, size_t pitch,
+                           int box_rows, int kbs) {
+  const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 128)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), 128u};
+  const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kbs)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -584,6 +606,7 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
     pl->pub.cluster = pair ? 2 : 1;
     pl->pub.threads = pair ? tc2_threads(pl->tc.epi) : tc_threads(realign);
     pl->pub.epilogue_warps = pair ? pl->tc.epi : 4;
+    pl->pub.kblocks_per_stage = pair ? 2 : 1;
     pl->pub.smem_bytes = pair ? tc2_smem_bytes(pl->tc.bn, pl->tc.stages, pl->tc.epi)
                               : tc_smem_bytes(pl->tc.bn, pl->tc.stages, realign);
     pl->pub.occupancy = 1;  // one CTA per SM: the ring fills shared memory
@@ -598,21 +621,53 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   const int num_kb = (K + 127) / 128;
   const int mp = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   const int n_tiles = (N + 127) / 128;
-  int best_s = 0, best_stages = 0, best_occ = 0;
+  int best_s = 0, best_stages = 0, best_occ = 0, best_kbs = 1;
   double best_cost = 1e300;
+  // Up to 32 tokens over a weight of at least 8 MB with K % 256 == 0: two K
+  // blocks per stage (3-D boxes), five stages (200 KB of loads in flight, one
+  // CTA per SM) and the most splits that keep every CTA on its own SM.
+  // Measured back to back against the single-K-block configurations the
+  // model below picks: 32 x 8192 x 8192 13.8 against 14.5 us (2 splits),
+  // 32 x 14336 x 4096 12.5 against 15.0 us (1 split, outputs stored straight
+  // from tensor memory), 16 x 4096 x 4096 9.8 against 12.2 us; with 64 tokens
+  // the 64-row stages leave room for four stages only and it is no faster.
+  const bool wide_auto = !o.tile_n && !o.stages && !o.splits && !realign && mp == 32 &&
+                         K % 256 == 0 && static_cast<long long>(N) * K >= (8LL << 20) &&
+                         dec_config_supported(32, 5, false, 2);
+  if (wide_auto) {
+    const int occ = dec_occupancy(d, 32, 5, false, 2);
+    for (int sp = 8; sp >= 1 && occ > 0; sp /= 2) {
+      if (num_kb % (2 * sp) != 0 || static_cast<long long>(n_tiles) * sp > d.sm_count) continue;
+      if (dec_clusters(d, 32, 5, false, 2, sp) * occ < n_tiles) continue;  // one wave
+      best_s = sp;
+      best_stages = 5;
+      best_occ = occ;
+      best_kbs = 2;
+      break;
+    }
+  }
+  // Several K blocks per stage (3-D boxes) need K % 128 == 0 (the boxes'
+  // view of a row ends exactly at its last byte) and TMA-readable operands;
+  // fp8gemm_options.tile_n selects the count on this path (0: automatic).
+  if (o.tile_n && o.tile_n != 1 && o.tile_n != 2 && o.tile_n != 4) return FP8GEMM_EINVAL;
+  for (int kbs : kDecKbs) {
+    if (best_s) break;  // chosen above
+    if (o.tile_n && kbs != o.tile_n) continue;
+    if (kbs > 1 && (realign || K % 128 != 0)) continue;
   for (int stages : kDecStages) {
     if (o.stages && stages != o.stages) continue;
-    if (!dec_config_supported(mp, stages, realign)) continue;
-    const int occ = dec_occupancy(d, mp, stages, realign);
+    if (!dec_config_supported(mp, stages, realign, kbs)) continue;
+    const int occ = dec_occupancy(d, mp, stages, realign, kbs);
     if (occ <= 0) continue;
-    const int s_max = std::max(1, std::min(8, num_kb));
+    const int s_max = std::max(1, std::min(8, num_kb / kbs));
     for (int s = 1; s <= s_max; ++s) {
       if (o.splits && s != o.splits) continue;
+      if (kbs > 1 && num_kb % (s * kbs) != 0) continue;  // whole stages per split
       // cudaOccupancyMaxActiveClusters answers as if one CTA per SM (the same
       // count for every ring depth); clusters of CTAs that fit `occ` to an SM
       // do share SMs (4 splits x 4 stages, 64 clusters of 4 on 152 SMs, ran
       // in one wave), so the count scales with occ.
-      const int clusters = dec_clusters(d, mp, stages, realign, s) * occ;
+      const int clusters = dec_clusters(d, mp, stages, realign, kbs, s) * occ;
       if (clusters <= 0) continue;
       // The weight stream is shared by the SMs: a wave costs the K blocks of
       // its busiest SM (CTAs per SM x K blocks per CTA), more when some SMs
@@ -628,8 +683,8 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
       const double coverage =
           static_cast<double>(std::min<long long>(grid, d.sm_count)) / d.sm_count;
       const double in_flight = static_cast<double>(per_sm) * stages *
-                               dec_stage_bytes(mp) / (160.0 * 1024.0);
-      const double cost =
+                               dec_stage_bytes(mp, kbs) / (160.0 * 1024.0);
+      double cost =
           static_cast<double>(waves) *
               (per_cta * per_sm * (1.0 + 0.5 * std::max(0.0, 1.0 - in_flight)) /
                    std::sqrt(coverage) +
@@ -640,8 +695,10 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
         best_s = s;
         best_stages = stages;
         best_occ = occ;
+        best_kbs = kbs;
       }
     }
+  }
   }
   if (best_s == 0) return FP8GEMM_EUNSUPPORTED;
   pl->dec.mp = mp;
@@ -649,6 +706,7 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   pl->dec.realign = realign;
   pl->dec.splits = best_s;
   pl->dec.n_tiles = n_tiles;
+  pl->dec.kbs = best_kbs;
   pl->pub.tile_m = 128;
   pl->pub.tile_n = mp;
   pl->pub.stages = best_stages;
@@ -656,7 +714,8 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   pl->pub.grid = n_tiles * best_s;
   pl->pub.cluster = best_s;
   pl->pub.threads = dec_threads(realign);
-  pl->pub.smem_bytes = dec_smem_bytes(mp, best_stages, realign);
+  pl->pub.smem_bytes = dec_smem_bytes(mp, best_stages, realign, best_kbs);
+  pl->pub.kblocks_per_stage = best_kbs;
   pl->pub.occupancy = best_occ;
   return FP8GEMM_OK;
 }
@@ -735,9 +794,15 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const v
       e = launch_tc(tmA, tmB, a, pl.tc, s);
     }
   } else {
-    if (use_tma && (encode_operand(&tmA, wa, N, K, lwa, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, xa, M, K, lxa, pl.dec.mp) != FP8GEMM_OK))
-      return FP8GEMM_ELAUNCH;
+    if (use_tma) {
+      const bool wide = pl.dec.kbs > 1;
+      if (wide ? (encode_operand_kblocks(&tmA, wa, N, K, lwa, 128, pl.dec.kbs) != FP8GEMM_OK ||
+                  encode_operand_kblocks(&tmB, xa, M, K, lxa, pl.dec.mp, pl.dec.kbs) !=
+                      FP8GEMM_OK)
+               : (encode_operand(&tmA, wa, N, K, lwa, 128) != FP8GEMM_OK ||
+                  encode_operand(&tmB, xa, M, K, lxa, pl.dec.mp) != FP8GEMM_OK))
+        return FP8GEMM_ELAUNCH;
+    }
     e = launch_decode(tmA, tmB, a, pl.dec, s);
   }
   if (e != cudaSuccess) {

@@ -48,10 +48,17 @@ __host__ __device__ constexpr int issuers_for() {
   return STAGES % 4 == 0 ? 4 : (STAGES % 3 == 0 ? 3 : (STAGES % 2 == 0 ? 2 : 1));
 }
 
-template <int MP, int STAGES, bool REALIGN>
+// KBS: 128-byte K blocks per pipeline stage.  KBS > 1 loads the stage's w
+// rows and x rows with one 3-D TMA box each (128 bytes x rows x KBS K
+// blocks; the tensor maps step K blocks 128 bytes apart), which lands as KBS
+// ordinary 128-byte-swizzled K-major tiles: one large copy per stage streams
+// the weight with far fewer, larger transfers.
+template <int MP, int STAGES, bool REALIGN, int KBS = 1>
 struct DCfg {
-  static constexpr int kABytes = kBN * kBK;
-  static constexpr int kBBytes = MP * kBK;
+  static constexpr int kABytes1 = kBN * kBK;  // one K block of w rows
+  static constexpr int kBBytes1 = MP * kBK;   // one K block of x rows
+  static constexpr int kABytes = kABytes1 * KBS;
+  static constexpr int kBBytes = kBBytes1 * KBS;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kPartBytes = kBN * MP * 4;
   static constexpr int kDataBytes =
@@ -64,14 +71,16 @@ struct DCfg {
   static constexpr int kSmemBytes = 1024 + kScaleOff + kBN * 4;
   static constexpr int kTmemCols = tmem_cols_for<MP>();
   static_assert(MP % 32 == 0 && MP >= 32 && MP <= 256, "MP");
+  static_assert(KBS == 1 || !REALIGN, "the realigning loader fills one K block per stage");
+  static_assert(kABytes1 % 1024 == 0 && kBBytes1 % 1024 == 0, "K-block tiles on 1024-byte atoms");
 };
 
-template <int MP, int STAGES, bool REALIGN>
+template <int MP, int STAGES, bool REALIGN, int KBS = 1>
 __global__ void __launch_bounds__(kThreads)
     fp8_linear_decode_kernel(const __grid_constant__ CUtensorMap tmW,
                              const __grid_constant__ CUtensorMap tmX, const GemmArgs p,
                              const int splits) {
-  using C = DCfg<MP, STAGES, REALIGN>;
+  using C = DCfg<MP, STAGES, REALIGN, KBS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -100,6 +109,11 @@ __global__ void __launch_bounds__(kThreads)
   const int kb_begin = static_cast<int>((static_cast<long long>(p.num_kb) * rank) / splits);
   const int kb_end = static_cast<int>((static_cast<long long>(p.num_kb) * (rank + 1)) / splits);
   const int my_kb = kb_end - kb_begin;
+  // pipeline stages of this CTA (the host makes my_kb a multiple of KBS)
+  const int my_it = my_kb / KBS;
+  // one split: the CTA owns whole outputs and stores them straight from
+  // tensor memory (no parking, no cluster reduction)
+  const bool direct = splits == 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -120,9 +134,11 @@ __global__ void __launch_bounds__(kThreads)
   // boxes instead gained less, 14.9 us).
   if (!REALIGN && lane == 0 && static_cast<int>(warp) < issuers_for<STAGES>()) {
     tma_prefetch_desc(&tmW);
-    const int pf = my_kb < STAGES ? my_kb : STAGES;
-    for (int i = static_cast<int>(warp); i < pf; i += issuers_for<STAGES>())
-      tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBK, n0);
+    const int pf = my_it < STAGES ? my_it : STAGES;
+    for (int i = static_cast<int>(warp); i < pf; i += issuers_for<STAGES>()) {
+      if constexpr (KBS == 1) tma_prefetch_l2_2d(&tmW, (kb_begin + i) * kBK, n0);
+      else tma_prefetch_l2_3d(&tmW, 0, n0, kb_begin + i * KBS);
+    }
   }
   // Global memory (operands, scales, y) is read or written only after the
   // preceding grids of the stream have completed; the set-up above overlaps
@@ -159,14 +175,19 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t pol_keep = l2_policy_evict_last();
         int last_use[STAGES];
         for (int s = 0; s < STAGES; ++s) last_use[s] = -1;
-        for (int i = static_cast<int>(warp); i < my_kb; i += kIssuers) {
+        for (int i = static_cast<int>(warp); i < my_it; i += kIssuers) {
           const int stage = i % STAGES;
           const uint32_t use = static_cast<uint32_t>(i / STAGES);
           if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) break;
           mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-          const int kb = kb_begin + i;
-          tma_load_2d_hint(sA(stage), &tmW, full_bar(stage), kb * kBK, n0, pol_stream);
-          tma_load_2d_hint(sB(stage), &tmX, full_bar(stage), kb * kBK, 0, pol_keep);
+          const int kb = kb_begin + i * KBS;
+          if constexpr (KBS == 1) {
+            tma_load_2d_hint(sA(stage), &tmW, full_bar(stage), kb * kBK, n0, pol_stream);
+            tma_load_2d_hint(sB(stage), &tmX, full_bar(stage), kb * kBK, 0, pol_keep);
+          } else {
+            tma_load_3d_hint(sA(stage), &tmW, full_bar(stage), 0, n0, kb, pol_stream);
+            tma_load_3d_hint(sB(stage), &tmX, full_bar(stage), 0, 0, kb, pol_keep);
+          }
           last_use[stage] = static_cast<int>(use);
         }
         for (int s = 0; s < STAGES; ++s)
@@ -206,7 +227,32 @@ __global__ void __launch_bounds__(kThreads)
         n0 + static_cast<int>(n_local) < p.N ? __ldg(p.scale + n0 + n_local) : 0.f;
     const bool have_acc = (my_kb == 0) || mbar_wait_bounded(acc_full_bar, 0u, wc, kErrWaitEpilogue);
     scale_s[n_local] = my_scale;
-    if (have_acc) {
+    if (have_acc && direct) {
+      // lane = output channel n, TMEM column = token m: y[m][n] for the
+      // warp's 32 channels, one coalesced 64-byte row segment per m
+      tc_fence_after_sync();
+      const int n = n0 + static_cast<int>(n_local);
+#pragma unroll 1
+      for (int c = 0; c < MP / 32; ++c) {
+        uint32_t v[32];
+        if (my_kb > 0) {
+          tmem_ld_32x32b_x32(tmem_base + ((warp * 32u) << 16) + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = c * 32 + j;
+            if (m < p.M)
+              p.y[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = static_cast<uint16_t>(
+                  pack_bf16x2(__uint_as_float(v[j]) * my_scale, 0.f) & 0xFFFFu);
+          }
+        }
+      }
+    } else if (have_acc) {
       tc_fence_after_sync();
 #pragma unroll 1
       for (int c = 0; c < MP / 32; ++c) {
@@ -230,7 +276,7 @@ __global__ void __launch_bounds__(kThreads)
       constexpr uint32_t kIdesc = idesc_e4m3_f32(kBN, MP);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int kb = kb_begin; kb < kb_end; ++kb) {
+      for (int i = 0; i < my_it; ++i) {
         if (!mbar_wait_bounded(full_bar(stage), phase, wc, kErrWaitMma)) {
           ok = false;
           break;
@@ -238,12 +284,15 @@ __global__ void __launch_bounds__(kThreads)
         // TMA data reach the MMA through the full barrier alone; operands written
         // by producer threads (generic proxy) additionally need the tcgen05 fence
         if (REALIGN) tc_fence_after_sync();
-        const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage));
-        const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage));
 #pragma unroll
-        for (int k = 0; k < kBK / kMmaK; ++k)
-          tc_mma_f8(tmem_base, a_desc + 2u * k, b_desc + 2u * k, kIdesc,
-                    (kb > kb_begin || k > 0) ? 1u : 0u);
+        for (int j = 0; j < KBS; ++j) {
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA(stage) + j * C::kABytes1);
+          const uint64_t b_desc = sdesc_kmajor_sw128(sB(stage) + j * C::kBBytes1);
+#pragma unroll
+          for (int k = 0; k < kBK / kMmaK; ++k)
+            tc_mma_f8(tmem_base, a_desc + 2u * k, b_desc + 2u * k, kIdesc,
+                      (i > 0 || j > 0 || k > 0) ? 1u : 0u);
+        }
         tc_commit(empty_bar(stage));
         if (++stage == STAGES) {
           stage = 0;
@@ -264,8 +313,8 @@ __global__ void __launch_bounds__(kThreads)
   // takes two float4 groups at a time and issues all their remote loads
   // before it sums any, so each round pays one remote latency.
   tc_fence_before_sync();
-  cluster_sync_all();
-  {
+  if (!direct) {
+    cluster_sync_all();
     const int groups = p.M * (kBN / 4);  // float4 groups of valid rows
     const int g_begin = static_cast<int>((static_cast<long long>(groups) * rank) / splits);
     const int g_end = static_cast<int>((static_cast<long long>(groups) * (rank + 1)) / splits);
@@ -327,14 +376,16 @@ __global__ void __launch_bounds__(kThreads)
 struct DEntry {
   int mp, stages;
   bool realign;
+  int kbs;
   const void* fn;
   int smem;
 };
 
-template <int MP, int S, bool R>
+template <int MP, int S, bool R, int KBS = 1>
 DEntry make_dentry() {
-  return DEntry{MP, S, R, reinterpret_cast<const void*>(&fp8_linear_decode_kernel<MP, S, R>),
-                DCfg<MP, S, R>::kSmemBytes};
+  return DEntry{MP, S, R, KBS,
+                reinterpret_cast<const void*>(&fp8_linear_decode_kernel<MP, S, R, KBS>),
+                DCfg<MP, S, R, KBS>::kSmemBytes};
 }
 
 const DEntry kDEntries[] = {
@@ -345,22 +396,25 @@ const DEntry kDEntries[] = {
     make_dentry<128, 4, false>(), make_dentry<256, 2, false>(), make_dentry<256, 3, false>(),
     make_dentry<256, 4, false>(), make_dentry<32, 3, true>(),   make_dentry<32, 4, true>(),
     make_dentry<64, 3, true>(),   make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
+    // several K blocks per stage (3-D boxes): one large copy of w per stage
+    make_dentry<32, 2, false, 4>(), make_dentry<32, 4, false, 2>(), make_dentry<32, 5, false, 2>(),
+    make_dentry<64, 2, false, 4>(), make_dentry<64, 4, false, 2>(),
 };
 
-const DEntry* dfind(int mp, int stages, bool realign) {
+const DEntry* dfind(int mp, int stages, bool realign, int kbs) {
   for (const DEntry& e : kDEntries)
-    if (e.mp == mp && e.stages == stages && e.realign == realign) return &e;
+    if (e.mp == mp && e.stages == stages && e.realign == realign && e.kbs == kbs) return &e;
   return nullptr;
 }
 
 }  // namespace
 
-bool dec_config_supported(int mp, int stages, bool realign) {
-  return dfind(mp, stages, realign) != nullptr;
+bool dec_config_supported(int mp, int stages, bool realign, int kbs) {
+  return dfind(mp, stages, realign, kbs) != nullptr;
 }
 
-int dec_smem_bytes(int mp, int stages, bool realign) {
-  const DEntry* e = dfind(mp, stages, realign);
+int dec_smem_bytes(int mp, int stages, bool realign, int kbs) {
+  const DEntry* e = dfind(mp, stages, realign, kbs);
   return e ? e->smem : -1;
 }
 
@@ -368,10 +422,10 @@ int dec_threads(bool) { return kThreads; }
 
 int dec_tmem_cols(int mp) { return mp <= 32 ? 32 : (mp <= 64 ? 64 : (mp <= 128 ? 128 : 256)); }
 
-int dec_stage_bytes(int mp) { return (kBN + mp) * kBK; }
+int dec_stage_bytes(int mp, int kbs) { return (kBN + mp) * kBK * kbs; }
 
-cudaError_t dec_prepare(int mp, int stages, bool realign) {
-  const DEntry* e = dfind(mp, stages, realign);
+cudaError_t dec_prepare(int mp, int stages, bool realign, int kbs) {
+  const DEntry* e = dfind(mp, stages, realign, kbs);
   if (!e) return cudaErrorInvalidValue;
   cudaError_t r =
       cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e->smem);
@@ -385,8 +439,8 @@ cudaError_t dec_prepare(int mp, int stages, bool realign) {
 // Resident CTAs per SM, counted from the kernel's resources: shared memory
 // (228 KB per SM, 1 KB of it reserved per CTA), registers (allocated per warp
 // in units of 256), threads (2048 per SM) and the 32-CTA limit.
-cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out) {
-  const DEntry* e = dfind(mp, stages, realign);
+cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int kbs, int* out) {
+  const DEntry* e = dfind(mp, stages, realign, kbs);
   if (!e) return cudaErrorInvalidValue;
   cudaFuncAttributes fa;
   cudaError_t r = cudaFuncGetAttributes(&fa, e->fn);
@@ -403,9 +457,9 @@ cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out) {
   return cudaSuccess;
 }
 
-cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,
-                                    int* out) {
-  const DEntry* e = dfind(mp, stages, realign);
+cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int kbs, int splits,
+                                    int grid, int* out) {
+  const DEntry* e = dfind(mp, stages, realign, kbs);
   if (!e) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -423,8 +477,10 @@ cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits
 
 cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                           const DecConfig& c, cudaStream_t s) {
-  const DEntry* e = dfind(c.mp, c.stages, c.realign);
+  const DEntry* e = dfind(c.mp, c.stages, c.realign, c.kbs);
   if (!e) return cudaErrorInvalidValue;
+  // every split must cover whole stages
+  if (c.kbs > 1 && (a.num_kb % (c.splits * c.kbs)) != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c.n_tiles * c.splits));
   cfg.blockDim = dim3(kThreads);

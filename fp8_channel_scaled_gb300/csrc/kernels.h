@@ -87,16 +87,17 @@ struct DecConfig {
   bool realign;    // operands loaded by the realigning producer instead of TMA
   int splits;      // K splits = cluster size (1..8)
   int n_tiles;     // ceil(N / 128)
+  int kbs;         // 128-byte K blocks per stage (> 1: 3-D tensor maps, K % 128 == 0)
 };
-bool dec_config_supported(int mp, int stages, bool realign);
-int dec_smem_bytes(int mp, int stages, bool realign);
+bool dec_config_supported(int mp, int stages, bool realign, int kbs);
+int dec_smem_bytes(int mp, int stages, bool realign, int kbs);
 int dec_threads(bool realign);
 int dec_tmem_cols(int mp);
-int dec_stage_bytes(int mp);  // shared-memory bytes of one ring stage (TMA path)
-cudaError_t dec_prepare(int mp, int stages, bool realign);
-cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int* out);
-cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int splits, int grid,
-                                    int* out);
+int dec_stage_bytes(int mp, int kbs);  // shared-memory bytes of one ring stage (TMA path)
+cudaError_t dec_prepare(int mp, int stages, bool realign, int kbs);
+cudaError_t dec_blocks_per_sm(int mp, int stages, bool realign, int kbs, int* out);
+cudaError_t dec_max_active_clusters(int mp, int stages, bool realign, int kbs, int splits,
+                                    int grid, int* out);
 cudaError_t launch_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                           const DecConfig& c, cudaStream_t s);
 

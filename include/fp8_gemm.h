@@ -68,7 +68,7 @@ extern "C" {
  * (identical to cudaStream_t). */
 typedef struct CUstream_st *fp8gemm_stream_t;
 
-#define FP8GEMM_VERSION 5
+#define FP8GEMM_VERSION 6
 
 typedef enum {
     FP8GEMM_OK = 0,
@@ -101,7 +101,10 @@ typedef struct {
     int force_realign;  /* 1: load operands with the in-kernel realigning
                            producer even when TMA could (tests that loader) */
     int tile_n;         /* main path N tile: 0 auto, or 128, 160, 192, 224, 256;
-                           64 with one-CTA tiles only */
+                           64 with one-CTA tiles only.  Decode path: 128-byte K
+                           blocks per pipeline stage, 0 auto, 1, 2 or 4 (2 and 4
+                           read each stage with one 3-D TMA box and need
+                           K % 128 == 0 and rows TMA can read in place) */
     int stages;         /* pipeline depth: 0 auto */
     int splits;         /* decode path K splits (cluster size): 0 auto, 1..8 */
     int no_workspace;   /* 1: never repitch; rows TMA cannot tile are then
@@ -151,6 +154,8 @@ typedef struct {
                            fp32 partial sum that the tile's owner adds */
     size_t workspace_bytes; /* device workspace the call needs (0 = none) */
     int epilogue_warps; /* warps scaling and storing y per CTA (4 or 8) */
+    int kblocks_per_stage; /* 128-byte K blocks per pipeline stage (decode: 1, 2 or
+                              4; main path: 2 on CTA pairs, 1 on one CTA) */
 } fp8gemm_plan;
 
 /*

@@ -329,6 +329,50 @@ def test_decode_splits(splits):
     check_full(x, w, s, Options(path=PATH_DECODE, splits=splits), what=f"splits {splits}")
 
 
+@pytest.mark.parametrize("M,N,K,kbs,stages,splits", [
+    (32, 4096, 4096, 2, 5, 1), (32, 4096, 4096, 2, 5, 2), (32, 4096, 4096, 4, 2, 4),
+    (17, 1000, 2048, 2, 4, 2), (1, 256, 1024, 4, 2, 1), (32, 640, 512, 2, 5, 2),
+    (64, 1024, 2048, 4, 2, 2), (50, 300, 1024, 2, 4, 1), (32, 128, 256, 2, 5, 1),
+])
+def test_decode_several_k_blocks_per_stage(M, N, K, kbs, stages, splits):
+    # Stages of 2 or 4 K blocks read with 3-D boxes (one per operand and
+    # stage) land as ordinary K-major tiles: every output equals the oracle's
+    # within the tolerance, with one split (outputs stored straight from
+    # tensor memory) or several (cluster reduction)
+    x, w, s = synth.make_inputs(M, N, K, seed=M * 7 + kbs)
+    o = Options(path=PATH_DECODE, tile_n=kbs, stages=stages, splits=splits)
+    p = fg.plan(M, N, K, o)
+    assert p.kblocks_per_stage == kbs and p.stages == stages and p.splits == splits
+    check_full(x, w, s, o, what=f"decode {M}x{N}x{K} kbs {kbs} stages {stages} splits {splits}")
+
+
+@pytest.mark.parametrize("kbs,stages", [(2, 5), (4, 2)])
+def test_decode_k_block_grouping_keeps_the_accumulation_order(kbs, stages):
+    # one split accumulates the K blocks in order in one accumulator, however
+    # many of them a stage holds: bitwise the same as one K block per stage
+    M, N, K = 32, 2048, 4096
+    x, w, s = synth.make_inputs(M, N, K, seed=61)
+    a = run(x, w, s, Options(path=PATH_DECODE, tile_n=kbs, stages=stages, splits=1))
+    b = run(x, w, s, Options(path=PATH_DECODE, tile_n=1, stages=4, splits=1))
+    assert np.array_equal(a, b)
+    compare(a, oracle.linear(x, w, s), f"kbs {kbs} single split")
+
+
+def test_decode_workload_plan_and_k_block_rules():
+    p = fg.plan(32, 8192, 8192)
+    assert p.path == PATH_DECODE and p.kblocks_per_stage == 2 and p.stages == 5 and p.splits == 2
+    assert fg.plan(32, 14336, 4096).splits == 1
+    # several K blocks per stage need K % 128 == 0: otherwise nothing is built
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.plan(32, 1024, 4100, Options(path=PATH_DECODE, tile_n=2))
+    assert e.value.status == 6
+    with pytest.raises(fg.FP8GemmError) as e:
+        fg.plan(32, 1024, 4096, Options(path=PATH_DECODE, tile_n=3))
+    assert e.value.status == 1
+    # small weights keep one K block per stage
+    assert fg.plan(32, 128, 256).kblocks_per_stage == 1
+
+
 @pytest.mark.parametrize("M", [8, 40, 128])
 def test_decode_realign(M):
     x, w, s = synth.make_inputs(M, 384, 1040, seed=M)

@@ -54,7 +54,7 @@ def test_header_compiles_as_c():
 
 def test_version_and_status_strings(cdll):
     import fp8_channel_scaled_gb300 as f
-    assert f.fp8_gemm_version() == 5
+    assert f.fp8_gemm_version() == 6
     for s in range(9):
         assert f.fp8_gemm_status_string(s) and f.fp8_gemm_status_string(s) != "unknown status"
     assert f.fp8_gemm_status_string(99) == "unknown status"
