@@ -623,31 +623,37 @@ int make_plan(DevState& d, const void* x, const void* w, int M, int N, int K,
   const int n_tiles = (N + 127) / 128;
   int best_s = 0, best_stages = 0, best_occ = 0, best_kbs = 1;
   double best_cost = 1e300;
-  // Up to 32 tokens over a weight of at least 8 MB with K % 256 == 0: two K
-  // blocks per stage (3-D boxes), five stages (200 KB of loads in flight, one
-  // CTA per SM) and the most splits that keep every CTA on its own SM.
-  // Measured back to back against the single-K-block configurations the
-  // model below picks: 32 x 8192 x 8192 13.8 against 14.5 us (2 splits),
-  // 32 x 14336 x 4096 12.5 against 15.0 us (1 split, outputs stored straight
-  // from tensor memory), 16 x 4096 x 4096 9.8 against 12.2 us; with 64 tokens
-  // the 64-row stages leave room for four stages only and it is no faster.
-  const bool wide_auto = !o.tile_n && !o.stages && !o.splits && !realign && mp == 32 &&
+  // Up to 128 tokens over a weight of at least 8 MB with K % 256 == 0: two K
+  // blocks per stage (3-D boxes), as many stages as fit one CTA per SM (5, 4
+  // and 3 for x tiles of 32, 64 and 128 rows: ~200 KB of loads in flight)
+  // and the most splits that keep every CTA on its own SM.  Measured back to
+  // back against the single-K-block configurations the model below picks:
+  // 32 x 8192 x 8192 13.8 against 14.5 us (2 splits), 32 x 14336 x 4096
+  // 12.5 against 15.0 us (1 split, outputs stored straight from tensor
+  // memory), 16 x 4096 x 4096 9.8 against 12.2 us, 64 x 4096 x 4096 8.7
+  // against 10.2 us, 64 x 14336 x 4096 14.7 against 17.1 us, 128 x 8192 x
+  // 8192 18.6 against 21.8 us; 64 x 8192 x 8192 16.1 against 15.9 us and 128
+  // x 4096 x 4096 9.6 against 9.8 us are about even, 192 and 256 tokens gain
+  // nothing and keep the model's choice.
+  const int wide_stages = mp == 32 ? 5 : (mp == 64 ? 4 : (mp == 128 ? 3 : 0));
+  const bool wide_auto = !o.tile_n && !o.stages && !o.splits && !realign && wide_stages > 0 &&
                          K % 256 == 0 && static_cast<long long>(N) * K >= (8LL << 20) &&
-                         dec_config_supported(32, 5, false, 2);
+                         dec_config_supported(mp, wide_stages, false, 2);
   if (wide_auto) {
-    const int occ = dec_occupancy(d, 32, 5, false, 2);
+    const int occ = dec_occupancy(d, mp, wide_stages, false, 2);
     for (int sp = 8; sp >= 1 && occ > 0; sp /= 2) {
       if (num_kb % (2 * sp) != 0 || static_cast<long long>(n_tiles) * sp > d.sm_count) continue;
-      if (dec_clusters(d, 32, 5, false, 2, sp) * occ < n_tiles) continue;  // one wave
+      if (dec_clusters(d, mp, wide_stages, false, 2, sp) * occ < n_tiles) continue;  // one wave
       best_s = sp;
-      best_stages = 5;
+      best_stages = wide_stages;
       best_occ = occ;
       best_kbs = 2;
       break;
     }
   }
-  // Several K blocks per stage (3-D boxes) need K % 128 == 0 (the boxes'
-  // view of a row ends exactly at its last byte) and TMA-readable operands;
+  // Otherwise every configuration is costed by the model below.  Several K
+  // blocks per stage (3-D boxes) need K % 128 == 0 (the boxes' view of a row
+  // ends exactly at its last byte) and TMA-readable operands;
   // fp8gemm_options.tile_n selects the count on this path (0: automatic).
   if (o.tile_n && o.tile_n != 1 && o.tile_n != 2 && o.tile_n != 4) return FP8GEMM_EINVAL;
   for (int kbs : kDecKbs) {

@@ -398,7 +398,8 @@ const DEntry kDEntries[] = {
     make_dentry<64, 3, true>(),   make_dentry<64, 4, true>(),   make_dentry<128, 2, true>(),
     // several K blocks per stage (3-D boxes): one large copy of w per stage
     make_dentry<32, 2, false, 4>(), make_dentry<32, 4, false, 2>(), make_dentry<32, 5, false, 2>(),
-    make_dentry<64, 2, false, 4>(), make_dentry<64, 4, false, 2>(),
+    make_dentry<64, 2, false, 4>(), make_dentry<64, 4, false, 2>(), make_dentry<128, 3, false, 2>(),
+    make_dentry<256, 2, false, 2>(),
 };
 
 const DEntry* dfind(int mp, int stages, bool realign, int kbs) {

@@ -333,6 +333,7 @@ def test_decode_splits(splits):
     (32, 4096, 4096, 2, 5, 1), (32, 4096, 4096, 2, 5, 2), (32, 4096, 4096, 4, 2, 4),
     (17, 1000, 2048, 2, 4, 2), (1, 256, 1024, 4, 2, 1), (32, 640, 512, 2, 5, 2),
     (64, 1024, 2048, 4, 2, 2), (50, 300, 1024, 2, 4, 1), (32, 128, 256, 2, 5, 1),
+    (100, 512, 1024, 2, 3, 2), (128, 384, 2048, 2, 3, 4), (200, 256, 512, 2, 2, 1),
 ])
 def test_decode_several_k_blocks_per_stage(M, N, K, kbs, stages, splits):
     # Stages of 2 or 4 K blocks read with 3-D boxes (one per operand and
@@ -362,6 +363,10 @@ def test_decode_workload_plan_and_k_block_rules():
     p = fg.plan(32, 8192, 8192)
     assert p.path == PATH_DECODE and p.kblocks_per_stage == 2 and p.stages == 5 and p.splits == 2
     assert fg.plan(32, 14336, 4096).splits == 1
+    p = fg.plan(64, 4096, 4096)
+    assert p.kblocks_per_stage == 2 and p.stages == 4 and p.splits == 4
+    p = fg.plan(128, 8192, 8192)
+    assert p.path == PATH_DECODE and p.kblocks_per_stage == 2 and p.stages == 3 and p.splits == 2
     # several K blocks per stage need K % 128 == 0: otherwise nothing is built
     with pytest.raises(fg.FP8GemmError) as e:
         fg.plan(32, 1024, 4100, Options(path=PATH_DECODE, tile_n=2))
