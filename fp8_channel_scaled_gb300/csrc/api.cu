@@ -446,6 +446,7 @@ bool pdl_ok(cudaStream_t s) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 size_t align256(size_t v) { return (v + 255u) & ~static_cast<size_t>(255u); }
 
 // Main path tile choice.  For each N tile (with the deepest ring that fits)
@@ -788,8 +789,16 @@ int launch_gemm(const Plan& pl, DevState& d, const void* xa, size_t lxa, const v
   if (pl.pub.path == FP8GEMM_PATH_MAIN) {
     // each CTA of a pair loads 128 rows of x and half of the tile's w rows
     const int b_rows = pl.tc.ctas == 2 ? pl.tc.bn / 2 : pl.tc.bn;
-    if (use_tma && (encode_operand(&tmA, xa, M, K, lxa, 128) != FP8GEMM_OK ||
-                    encode_operand(&tmB, wa, w_rows, K, lwa, b_rows) != FP8GEMM_OK))
+    // Pair tiles with four producers read each stage's two K blocks of an
+    // operand as one 3-D box when K % 128 == 0: half the TMA copies (square
+    // 44.8 -> 44.3 us, MLP 264.2 -> 262.9 us, 512 x 4096 x 4096 14.07 ->
+    // 13.84 us; interleaved A/B runs)
+    a.kbox = (use_tma && pl.tc.ctas == 2 && pl.tc.epi == 4 && K % 128 == 0) ? 1 : 0;
+    if (use_tma && (a.kbox ? (encode_operand_kblocks(&tmA, xa, M, K, lxa, 128, 2) != FP8GEMM_OK ||
+                              encode_operand_kblocks(&tmB, wa, w_rows, K, lwa, b_rows, 2) !=
+                                  FP8GEMM_OK)
+                           : (encode_operand(&tmA, xa, M, K, lxa, 128) != FP8GEMM_OK ||
+                              encode_operand(&tmB, wa, w_rows, K, lwa, b_rows) != FP8GEMM_OK)))
       return FP8GEMM_ELAUNCH;
     if (pl.tc.ctas == 2) {
       CUtensorMap tmY;

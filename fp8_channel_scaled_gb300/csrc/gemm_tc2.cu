@@ -237,7 +237,9 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), kKbPerStage == 2 ? 4u : 2u);  // CTA 0's producers of stage s
+      // CTA 0's producers of stage s: one per operand and K block, or one per
+      // operand when a 3-D box carries both K blocks
+      mbar_init(full_bar(s), kKbPerStage == 2 ? (p.kbox ? 2u : 4u) : 2u);
       mbar_init(empty_bar(s), 1u);
     }
     for (int a = 0; a < 2; ++a) {
@@ -318,6 +320,25 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
                              : tg.wrow + static_cast<int>(rank) * C::kBRows;
         for (int kb = wu.k0; kb < wu.k1; kb += kKbPerStage, ++it) {
           if (kKbPerStage == 1 && static_cast<int>(it & 1u) != sub) continue;
+          if (EPI == 4 && p.kbox) {
+            // one 3-D box carries both K blocks of this operand: the two
+            // producers of an operand take alternate stages (a producer
+            // never waits for a stage it does not load); a K block past the
+            // unit's end is loaded but not used (past K: read as zero)
+            if (static_cast<int>(it & 1u) != sub) continue;
+            const uint32_t stage = it % STAGES;
+            const uint32_t use = it / STAGES;
+            if (!mbar_wait_bounded(empty_bar(stage), (use & 1u) ^ 1u, wc, kErrWaitProducer)) {
+              ok = false;
+              break;
+            }
+            const uint32_t box = is_a ? C::kABytes : C::kBBytes;
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * box);
+            tma_load_3d_pair(sbase + stage * static_cast<uint32_t>(C::kStageBytes) +
+                                 (is_a ? 0u : static_cast<uint32_t>(C::kABytes)),
+                             map, mapa_shared(full_bar(stage), 0u), 0, row, kb);
+            continue;
+          }
           // An odd CTA's producer whose K block of this stage lies past the
           // unit's end (an odd number of K blocks) has nothing to load and
           // must not wait for the stage either: the MMA does not need it

@@ -37,6 +37,10 @@ struct GemmArgs {
   const int* group_offsets;  // device, groups + 1 entries
   int groups;
   int pdl;  // host side: launch with programmatic stream serialization
+  // CTA-pair kernel with four producer warps: 1 when each stage's two K
+  // blocks of an operand are one 3-D box (tensor maps [K / 128][rows][128
+  // bytes], K % 128 == 0), 0 when each K block is its own 2-D box
+  int kbox;
 };
 
 // ---- persistent tcgen05 kernel (large M) ---------------------------------
