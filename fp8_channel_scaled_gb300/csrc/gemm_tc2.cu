@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0u));
+      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0u));
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }

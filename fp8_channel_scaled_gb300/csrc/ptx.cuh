@@ -501,10 +501,15 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Arrive on an mbarrier given by its cluster address (possibly another CTA's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
+// Arrive on an mbarrier given by its cluster address (possibly another CTA's)
+// with the default semantics, release at CTA scope: the arrive orders nothing
+// of this thread's memory for the peer CTA.  It serves as the signal that this
+// warp's tensor-memory reads are over, and those are complete before it
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync).  A release at
+// cluster scope would first wait until every earlier write of the thread is
+// visible to the whole cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // ----------------------------------------------------------------------------
