@@ -70,10 +70,19 @@ struct Cfg2 {
   static constexpr int kBBytes = kKbPerStage * kBBytes1;
   static constexpr int kStageBytes = kABytes + kBBytes;  // [x kb0][x kb1][w kb0][w kb1]
   static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
-  static constexpr int kStgOff = STAGES * kStageBytes;            // EPI warps x 2 staging boxes
+  static constexpr int kStgOff = STAGES * kStageBytes;  // EPI warps x kBoxes staging boxes
   static constexpr int kNumBars = 2 * STAGES + 6 + kEpiWarps;  // + one per epilogue warp
+  // Staging boxes per epilogue warp: with eight warps, one per chunk of the
+  // warp where shared memory allows (no chunk then waits for an earlier
+  // store of the same tile to read its box), else two used in turn.
+  static constexpr int kBoxes =
+      (EPI == 8 && kSplit > 2 &&
+       1024 + kStgOff + kEpiWarps * kSplit * kStgBytes + kEpiWarps * BN * 4 + kNumBars * 8 + 16 <=
+           232448)
+          ? kSplit
+          : 2;
   // each epilogue warp's copy of the tile's BN scales, where it fits
-  static constexpr int kScOff = kStgOff + kEpiWarps * 2 * kStgBytes;
+  static constexpr int kScOff = kStgOff + kEpiWarps * kBoxes * kStgBytes;
   static constexpr bool kScInSmem =
       1024 + kScOff + kEpiWarps * BN * 4 + kNumBars * 8 + 16 <= 232448;
   static constexpr int kBarOff = kScOff + (kScInSmem ? kEpiWarps * BN * 4 : 0);
@@ -475,7 +484,8 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
     uint32_t acc = 0, acc_phase = 0, chunk_no = 0, part_phase = 0;
     const bool zero_acc = (num_kb == 0);
     const bool tma_y = p.vec_store != 0;
-    const uint32_t stg = sbase + static_cast<uint32_t>(C::kStgOff) + warp * 2u * kStgBytes;
+    const uint32_t stg =
+        sbase + static_cast<uint32_t>(C::kStgOff) + warp * static_cast<uint32_t>(C::kBoxes * kStgBytes);
     constexpr int kChunks = BN / 32;
     // TMEM lane quarter (= tile rows) and chunk range of this warp: all
     // chunks of its quarter with four epilogue warps, half of them with eight
@@ -647,40 +657,93 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
               }
             }
           };
-          // Chunks are handled in pairs (va, vb ping-pong): both are
-          // computed, then staged in the warp's two boxes once the previous
-          // pair's stores have read them, with one proxy fence for the two.
-          tmem_ld_32x32b_x32(t_row + c_lo * 32, va);
-#pragma unroll 1
-          for (int c = c_lo; c < c_hi; c += 2) {
-            const bool two = c + 1 < c_hi;
-            uint32_t pk0[16], pk1[16];
-            tmem_ld_wait();
-            if (two) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
-            compute(c, va, pk0);
-            if (two) {
-              tmem_ld_wait();
-              if (c + 2 < c_hi) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
-              compute(c + 1, vb, pk1);
+          if constexpr (C::kBoxes >= C::kSplit) {
+            // Every chunk of the warp has its own box, so only the previous
+            // tile's stores (issued a whole tile ago) must have read theirs
+            // before this tile's first chunk is staged; each pair of chunks
+            // is stored as soon as it is staged (storing all of them at the
+            // end, behind one proxy fence, or a pair through one 32 x 64 box
+            // with the 128-byte swizzle, was no faster).  A box straddling
+            // the end of the tile's group is stored row by row from
+            // registers instead.
+            const bool whole = row0 + 32 <= tg.row_end || tg.row_end >= p.M;
+            if (tma_y && chunk_no > 0) {
+              if (lane == 0) tma_store_wait_read<0>();
+              __syncwarp();
             }
-            if (tma_y) {
-              if (chunk_no > 0) {  // every earlier store has read its box
-                if (lane == 0) tma_store_wait_read<0>();
-                __syncwarp();
-              }
-              put(stg, pk0);
-              if (two) put(stg + kStgBytes, pk1);
+            auto stage = [&](int c, const uint32_t (&packed)[16]) {
+              if (tma_y && whole) put(stg + static_cast<uint32_t>(c - c_lo) * kStgBytes, packed);
+              else direct(c, packed);
+            };
+            // proxy fence, then the TMA stores of staged chunks [c0, c1)
+            auto flush = [&](int c0, int c1) {
+              if (!tma_y) return;
               fence_proxy_async_smem();
               __syncwarp();
-              emit_chunk(&tmY, stg, p, row0, tg.row_end, nb * BN + c * 32, lane, pk0);
-              if (two)
-                emit_chunk(&tmY, stg + kStgBytes, p, row0, tg.row_end, nb * BN + (c + 1) * 32,
-                           lane, pk1);
-            } else {
-              direct(c, pk0);
-              if (two) direct(c + 1, pk1);
+              if (lane == 0) {
+                for (int c = c0; c < c1; ++c) {
+                  const int col0 = nb * BN + c * 32;
+                  if (whole && row0 < p.M && col0 < p.N)
+                    tma_store_2d(&tmY, stg + static_cast<uint32_t>(c - c_lo) * kStgBytes, col0,
+                                 row0);
+                }
+                tma_store_commit();
+              }
+            };
+            tmem_ld_32x32b_x32(t_row + c_lo * 32, va);
+#pragma unroll 1
+            for (int c = c_lo; c < c_hi; c += 2) {
+              const bool two = c + 1 < c_hi;
+              uint32_t pk0[16], pk1[16];
+              tmem_ld_wait();
+              if (two) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+              compute(c, va, pk0);
+              stage(c, pk0);
+              if (two) {
+                tmem_ld_wait();
+                if (c + 2 < c_hi) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
+                compute(c + 1, vb, pk1);
+                stage(c + 1, pk1);
+              }
+              flush(c, two ? c + 2 : c + 1);
             }
-            chunk_no += two ? 2u : 1u;
+            chunk_no += static_cast<uint32_t>(c_hi - c_lo);
+          } else {
+            // Chunks are handled in pairs (va, vb ping-pong): both are
+            // computed, then staged in the warp's two boxes once the previous
+            // pair's stores have read them, with one proxy fence for the two.
+            tmem_ld_32x32b_x32(t_row + c_lo * 32, va);
+#pragma unroll 1
+            for (int c = c_lo; c < c_hi; c += 2) {
+              const bool two = c + 1 < c_hi;
+              uint32_t pk0[16], pk1[16];
+              tmem_ld_wait();
+              if (two) tmem_ld_32x32b_x32(t_row + (c + 1) * 32, vb);
+              compute(c, va, pk0);
+              if (two) {
+                tmem_ld_wait();
+                if (c + 2 < c_hi) tmem_ld_32x32b_x32(t_row + (c + 2) * 32, va);
+                compute(c + 1, vb, pk1);
+              }
+              if (tma_y) {
+                if (chunk_no > 0) {  // every earlier store has read its box
+                  if (lane == 0) tma_store_wait_read<0>();
+                  __syncwarp();
+                }
+                put(stg, pk0);
+                if (two) put(stg + kStgBytes, pk1);
+                fence_proxy_async_smem();
+                __syncwarp();
+                emit_chunk(&tmY, stg, p, row0, tg.row_end, nb * BN + c * 32, lane, pk0);
+                if (two)
+                  emit_chunk(&tmY, stg + kStgBytes, p, row0, tg.row_end, nb * BN + (c + 1) * 32,
+                             lane, pk1);
+              } else {
+                direct(c, pk0);
+                if (two) direct(c + 1, pk1);
+              }
+              chunk_no += two ? 2u : 1u;
+            }
           }
         } else {
           tmem_ld_32x32b_x32(t_row, va);
