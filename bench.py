@@ -249,13 +249,13 @@ def cpu_baseline(x, w, s, wl, target_s: float = 12.0, rows=None):
 
 def bench_workload(key, steps, warmup, device, l2_bytes, stream, fg, prepared_weight=False):
     """Time `steps` back-to-back calls of a workload.  prepared_weight: each
-    set's w is first copied once (outside the timed region) to a 16-byte row
+    set's w is first copied once (outside the timed region) to a 64-byte row
     pitch with fp8_gemm_prepare_weight, as a deployment that keeps its
     weights in that layout would."""
     import torch
     wl, host, sets, per_set = prepare(key, device, l2_bytes, rotate=(key != "small"))
     if prepared_weight:
-        kp = (wl.K + 15) // 16 * 16
+        kp = (wl.K + 63) // 64 * 64
         prepped = []
         for x, w, s, y in sets:
             buf = torch.empty((wl.N, kp), dtype=torch.uint8, device=device)
@@ -471,7 +471,7 @@ def run_ours(args):
             p2 = fg.plan(wl2.M, wl2.N, wl2.K, x=sets2[0][0], w=sets2[0][1])
             srcs2 = (DEC_SOURCES if p2.path == fg.PATH_DECODE
                      else TC2_SOURCES if p2.cluster == 2 else TC_SOURCES)
-            others[key2] = {"workload": wl2.name + (" (w prepared once to a 16-byte pitch; x repitched per call)" if key2 != base else ""),
+            others[key2] = {"workload": wl2.name + (" (w prepared once to a 64-byte pitch; x repitched per call)" if key2 != base else ""),
                             "us_per_call": round(k2 * 1e6, 2),
                            "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1),
                            "frac_roofline_nominal": round(roof_t / k2, 4),

@@ -1,13 +1,14 @@
 // repitch.cu -- copy the E4M3 operands x [M, K] and w [N, K], whose rows
 // are not 16-byte aligned (K % 16 != 0, or a base address that is not
-// 16-byte aligned), into a workspace whose rows are Kp = round_up(K, 16)
-// bytes long, with the Kp - K pad bytes set to zero.  The tile kernel then
+// 16-byte aligned), into a workspace whose rows are Kp bytes long (a multiple
+// of 16 >= K: the library takes round_up(K, 64)), with the Kp - K pad bytes
+// set to zero.  The tile kernel then
 // reads the copies through TMA, which needs 16-byte row pitches.
 //
 // This is the per-call zero-padding pass the pages' Blackwell submission runs
 // on live data ("Kimi K3 (256k)" page, sm_100 tcgen05 paragraph: K = 4127 is
 // padded to 4128 by a padding kernel on every forward, never cached), here
-// padding only to the next multiple of 16 bytes.  Zero bytes add exactly
+// padding only to the next multiple of 64 bytes.  Zero bytes add exactly
 // nothing to a dot product, so results equal the unpadded ones.
 //
 // One warp copies a segment of 64, 96 or 128 output chunks (the width that

@@ -145,7 +145,7 @@ typedef struct {
     int threads;        /* threads per CTA */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int launches;       /* kernels launched by one call (0, 1, or 2 with repitch) */
-    int repitch;        /* 1: operands are first copied to a 16-byte pitch */
+    int repitch;        /* 1: operands are first copied to a 64-byte pitch */
     int occupancy;      /* resident CTAs per SM of the GEMM kernel */
     int split_tiles;    /* main path, CTA pairs: tiles past the last full wave
                            whose K blocks are shared out between
@@ -170,7 +170,7 @@ typedef struct {
  *
  * Rows whose pitch K is not a multiple of 16 bytes (e.g. K = 4127), or
  * operands not 16-byte aligned, cannot be tiled by TMA.  They are first
- * copied by a repitch kernel into the workspace with a 16-byte pitch and zero
+ * copied by a repitch kernel into the workspace with a 64-byte pitch and zero
  * pad bytes (two launches); with no_workspace an in-kernel realigning
  * producer loads them directly instead (one launch, no workspace, but about
  * ten times slower on large shapes: its loads pass through registers).
@@ -231,7 +231,7 @@ size_t fp8_gemm_workspace_bytes(int device, const void *x, const void *w, int M,
  * library holds until the process exits.  The repitch kernel writes every
  * byte of it that the GEMM then reads, pad bytes included, so nothing has to
  * start at zero.  Calls that need more than that (M * Kp + N * Kp bytes,
- * Kp = round_up(K, 16), each part rounded up to 256 bytes) return
+ * Kp = round_up(K, 64), each part rounded up to 256 bytes) return
  * FP8GEMM_ESIZE and launch nothing.
  *
  * All calls on a device share the one array and it keeps the last call's
