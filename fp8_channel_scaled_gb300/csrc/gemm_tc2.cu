@@ -264,6 +264,32 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
   // Both CTAs' barriers are initialised before any cross-CTA arrive or TMA
   // completion.
   cluster_sync_all();
+  // Before the dependency wait, one producer per operand asks L2 for the
+  // first stage of this pair's first tile (cp.async.bulk.prefetch.tensor): a
+  // prefetch delivers nothing to the CTA and L2 is the point of coherence, so
+  // the loads issued after the wait still observe every write of the
+  // preceding grids.  The CTAs of a call become resident 1-3 us before the
+  // previous call's grid completes, and after the wait all of them used to
+  // ask DRAM for ~9 MB of first stages at once (first operands 2.4-3.7 us
+  // after the wait; globaltimer stamps, 4096^3).  One stage: square 45.0 ->
+  // 44.5 us, MLP 261.4 -> 260.5 us, 8192x8192x128 43.5 -> 42.9 us; two stages
+  // gained no more.  The tile comes from the plain raster, so grouped layers
+  // (whose tile map reads group offsets from memory) and split tails skip it.
+  if (p.group_offsets == nullptr && p.tail_workers == 0 && p.num_kb > 0 && warp >= kProdWarp0 &&
+      lane == 0 && ((warp - kProdWarp0) & 1u) == 0u && pair < num_m2_blk * num_n_blk) {
+    const bool is_a = (warp - kProdWarp0) < 2u;
+    int mb, nb;
+    tile_coords(pair, num_m2_blk, num_n_blk, group_m, mb, nb);
+    const int row =
+        is_a ? mb * 256 + static_cast<int>(rank) * 128 : nb * BN + static_cast<int>(rank) * C::kBRows;
+    const CUtensorMap* map = is_a ? &tmA : &tmB;
+    if (EPI == 4 && p.kbox) {
+      tma_prefetch_l2_3d(map, 0, row, 0);
+    } else {
+      tma_prefetch_l2_2d(map, 0, row);
+      if (p.num_kb > 1) tma_prefetch_l2_2d(map, kBK, row);
+    }
+  }
   // Global memory (operands, scales, y) is touched only after the preceding
   // grids of the stream have completed; the set-up above overlaps their tail.
   // Tensor memory is allocated only after the wait, so this CTA never holds
