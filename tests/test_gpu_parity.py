@@ -998,6 +998,25 @@ def test_grouped_layer_equals_separate_calls_on_exact_sums():
             assert np.array_equal(got[lo:hi], oracle.linear(x[lo:hi], w[g], s[g]))
 
 
+@pytest.mark.parametrize("bn", [256, 192])
+def test_grouped_layer_with_eight_epilogue_warps(bn):
+    # Eight epilogue warps with a staging box per chunk: 32-row output boxes
+    # that straddle a group's end are stored row by row, the others by TMA.
+    offs = [0, 45, 45, 301, 333, 700, 1000]
+    M, G, N, K = 1000, len(offs) - 1, 640, 256
+    x, _, _ = synth.make_inputs(M, 8, K, seed=91)
+    rng = np.random.default_rng(92)
+    w = np.stack([synth.make_inputs(8, N, K, seed=93 + g)[1] for g in range(G)])
+    s = (rng.uniform(0.5, 1.5, (G, N)) / np.sqrt(K)).astype(np.float32)
+    o8 = Options(mma_ctas=2, tile_n=bn, epilogue_warps=8)
+    got = run_grouped(x, w, s, offs, o8)
+    for g, (lo, hi) in enumerate(group_ranges(offs, M)):
+        if hi > lo:
+            compare(got[lo:hi], oracle.linear(x[lo:hi], w[g], s[g]), f"group {g}, bn {bn}")
+    assert np.array_equal(got, run_grouped(x, w, s, offs, Options(mma_ctas=2, tile_n=bn,
+                                                                   epilogue_warps=4)))
+
+
 def test_grouped_layer_argument_checks():
     M, G, N, K = 64, 2, 128, 200  # K % 16 != 0: not readable by TMA in place
     x = to_dev(np.zeros((M, K), np.uint8))
