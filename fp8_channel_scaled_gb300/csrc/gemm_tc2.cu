@@ -17,7 +17,10 @@
 // and MMA issue (even CTA, one thread), warps 5-8 TMA producers, one thread
 // each: x of a stage's first K block, x of its second, w of its first, w of
 // its second (a TMA copy keeps its issuing thread busy for about a hundred
-// cycles, so one thread per operand cannot keep the tensor cores fed).
+// cycles, so one thread per operand cannot keep the tensor cores fed); with
+// one 3-D box per operand and stage (K % 128 == 0) the two producers of an
+// operand take alternate stages.  Short-K shapes use eight epilogue warps
+// (0-7), the MMA warp 8 and three producers (9-11).
 //
 // A stage holds two 128-byte K blocks.  The issuing thread spends about 95
 // cycles per tcgen05.mma and about 70 per barrier wait even when the stage
@@ -25,11 +28,13 @@
 // wait and commit, issue rather than the tensor core set the pace; with two
 // (8 MMAs, 1024 cycles) per wait and commit it keeps ahead.
 // Synchronisation:
-//   full[s]   in CTA 0 only: CTA 0's four producers arm it, each with its
-//             box's bytes for both CTAs; both CTAs' loads complete on it;
+//   full[s]   in CTA 0 only: CTA 0's producers of the stage arm it, each
+//             with its box's bytes for both CTAs; both CTAs' loads complete
+//             on it;
 //   empty[s]  in both CTAs: the MMA commit multicasts to both;
 //   tfull[a]  in both CTAs: multicast commit after a tile's last K block;
-//   tempty[a] in CTA 0 only: all 8 epilogue warps of the pair arrive on it.
+//   tempty[a] in CTA 0 only: every epilogue warp of the pair (8 or 16)
+//             arrives on it.
 // Every wait is bounded, as in the one-CTA kernel.
 #include <cuda_bf16.h>
 
