@@ -263,8 +263,9 @@ def fp8_gemm_grouped(x, w, scale, y, offsets, options: Options | None = None, st
 
 def fp8_gemm_prepare_weight(w, w_out, stream=None):
     """Copy w [N, K] (contiguous) into the rows of w_out, a uint8 [N, ldw]
-    buffer (ldw a multiple of 16, >= K), zeroing bytes past K; returns the
-    [N, K] view of w_out to pass as w (its pitch reaches the library)."""
+    buffer (ldw a multiple of 16, >= K; a multiple of 64 reads fastest),
+    zeroing bytes past K; returns the [N, K] view of w_out to pass as w (its
+    pitch reaches the library)."""
     if w.dim() != 2 or not w.is_contiguous() or w.element_size() != 1:
         raise ValueError("w must be a contiguous 2-D 1-byte tensor")
     N, K = w.shape

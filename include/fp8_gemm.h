@@ -292,7 +292,10 @@ int fp8_gemm_grouped(const void *x, const void *w, const float *scale, void *y,
  * (the pages cache a padded weight per weight version: "glm-5.2" page,
  * Triton TMA paragraph; "Kimi K3 (256k)" page, sm_100 tcgen05 paragraph;
  * here the caller owns the copy and decides when it is stale, and the
- * default path keeps nothing between calls).  Asynchronous on `stream`; w_out must not overlap w.
+ * default path keeps nothing between calls).  A pitch that is a multiple of
+ * 64 bytes is the fast choice: rows an odd multiple of 16 bytes apart start
+ * every 128-byte K block in the middle of a 32-byte sector, which slows the
+ * GEMM by up to a sixth.  Asynchronous on `stream`; w_out must not overlap w.
  */
 int fp8_gemm_prepare_weight(const void *w, int N, int K, void *w_out, size_t ldw_out,
                             fp8gemm_stream_t stream);
