@@ -402,11 +402,13 @@ struct Plan {
   size_t part_off, flag_off;  // offsets of the split-tail partial sums and flags
 };
 
-// Most segments a split tile is cut into.  Its owner adds the other
+// Tail workers per tail tile, at most.  A split tile's owner adds the other
 // segments' partial sums (256 x BN x 4 bytes each) before it can write y; the
-// pair kernel stages one of them in shared memory, so two segments keep the
-// fix-up to one bulk copy.
-constexpr int kMaxSegmentsPerTile = 2;
+// pair kernel stages the first of them in shared memory and reads any further
+// one from L2.  With twice as many workers as tail tiles every range is half a
+// tile and a tile has two segments; with fewer (the pairs run out) the ranges
+// no longer follow tile boundaries and a tile may have three.
+constexpr int kTailWorkersPerTailTile = 2;
 
 // CTA pairs that share the split tail of `tiles` tiles on `pairs` pairs, or
 // 0 when splitting does not shorten the last wave.
@@ -414,7 +416,7 @@ int tail_workers_for(long long tiles, int pairs, int num_kb) {
   if (pairs <= 0 || num_kb <= 0) return 0;
   const long long rem = tiles % pairs;
   if (rem == 0) return 0;
-  long long tw = std::min<long long>(pairs, rem * kMaxSegmentsPerTile);
+  long long tw = std::min<long long>(pairs, rem * kTailWorkersPerTailTile);
   tw = std::min<long long>(tw, rem * num_kb);  // every range at least one K block
   return tw > rem ? static_cast<int>(tw) : 0;
 }

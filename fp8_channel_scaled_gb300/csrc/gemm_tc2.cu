@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(Cfg2<BN, STAGES, EPI>::kThreads, 1)
         // memory with one bulk copy: a tile with contributors is always its
         // owner's last unit, so the operand ring is idle (every MMA of the
         // pair has completed) and holds it.  Any further contributor (the
-        // host cuts tiles into at most two segments) is read from L2.
+        // ranges hold at least half a tile, so at most one more) is read from L2.
         bool have_parts = true;
         const bool staged = wu.q_end > pair + 1;
         if (staged) {

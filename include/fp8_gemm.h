@@ -180,7 +180,7 @@ typedef struct {
  *
  * With fp8gemm_options.split_tail on CTA-pair tiles, when the tiles do not
  * fill the last wave of the persistent grid, that wave's tiles are cut along
- * K into up to two segments run by different CTA pairs
+ * K into two or three segments run by different CTA pairs
  * (fp8gemm_plan.split_tiles).  Every pair then ends after about the same
  * number of K blocks.  The pair that holds a tile's first K block adds the
  * other segment's fp32 partial sum (published through the workspace) to its
